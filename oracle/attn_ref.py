@@ -1,0 +1,166 @@
+"""fp64 CPU oracle for exact softmax attention and its analytic backward pass.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` call it.  It shares no code with the
+CUDA kernels (no helpers, tables or constants) and performs the full-matrix
+computation with no tiling, fusion or reordering, so that each line can be
+checked by eye against the definitions below.
+
+Definitions (per batch b and query head h; the key/value head is
+h_kv = h // (Hq // Hkv), i.e. consecutive groups of query heads share one
+key/value head -- the plainest reading of the GQA support described in
+"[Kernel] Flash attention 2" (Liger-Kernel #275), "Details"):
+
+  S_ij  = scale * sum_c Q_ic K_jc, and S_ij = -inf when causal and j > i
+          (flash_attention_backward.cu, rustytorch rtx-flash-attention,
+          blocks "Recompute attention scores" and "Apply causal mask")
+  L_i   = log sum_j exp(S_ij)         natural log of the *scaled* scores
+          (same file, block "Compute softmax probabilities from scores and LSE")
+  P_ij  = exp(S_ij - L_i)             (same block)
+  O_i   = sum_j P_ij V_j
+  dV_j  = sum_i P_ij dO_i             (same file, block "Compute dV")
+  dP_ij = sum_c dO_ic V_jc            (same file, block "Compute dS", first step)
+  D_i   = sum_j P_ij dP_ij            (equal to sum_c dO_ic O_ic, which is the
+          form the pages precompute: same file, block "Compute row-wise dot
+          product: dO * O"; the Triton kernel in triton #1806 takes it as D)
+  dS_ij = P_ij (dP_ij - D_i)          (same file, block "Compute dS")
+  dQ_i  = scale * sum_j dS_ij K_j     (same file, block "Compute dQ")
+  dK_j  = scale * sum_i dS_ij Q_i     (same file, block "Compute dK")
+  GQA:  dK, dV of a key/value head are summed over the query heads of its group.
+
+All arithmetic is float64.  Inputs (16-bit on the CUDA side) are widened
+exactly to float64 before use.  Matrix products use numpy's matmul as a
+library primitive.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x) -> np.ndarray:
+    """Widen a torch tensor or array exactly to a float64 numpy array."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu().to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def kv_head(h: int, Hq: int, Hkv: int) -> int:
+    """Key/value head used by query head h: consecutive groups of Hq//Hkv."""
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return h // (Hq // Hkv)
+
+
+def scores(q: np.ndarray, k: np.ndarray, scale: float, causal: bool) -> np.ndarray:
+    """S = scale * Q K^T for one head, [Nq, Nkv], with the top-left causal mask.
+
+    Causal masking drops key j for query i whenever j > i (the literal rule
+    of the pages' CUDA kernel); with Nq == Nkv this is the usual mask.
+    """
+    s = scale * (q @ k.T)
+    if causal:
+        nq, nk = s.shape
+        i = np.arange(nq)[:, None]
+        j = np.arange(nk)[None, :]
+        s = np.where(j > i, -np.inf, s)
+    return s
+
+
+def logsumexp_rows(s: np.ndarray) -> np.ndarray:
+    """L_i = log sum_j exp(S_ij), evaluated stably as m_i + log sum_j exp(S_ij - m_i)."""
+    m = s.max(axis=1)
+    return m + np.log(np.exp(s - m[:, None]).sum(axis=1))
+
+
+def head_forward(q, k, v, scale, causal):
+    """Forward for one head: returns (O [Nq,d], L [Nq], P [Nq,Nkv])."""
+    s = scores(q, k, scale, causal)
+    lse = logsumexp_rows(s)
+    p = np.exp(s - lse[:, None])
+    return p @ v, lse, p
+
+
+def head_backward(q, k, v, do, scale, causal, lse=None, o=None):
+    """Backward for one head.
+
+    Returns a dict with dq [Nq,d], dk [Nkv,d], dv [Nkv,d], D [Nq] (the
+    rowsum(P * dP) form), D_rowdot [Nq] (the rowsum(dO * O) form, only when
+    ``o`` is given or computed), and dS [Nq,Nkv].
+
+    ``lse`` / ``o``: when given, P is formed from that log-sum-exp and
+    D_rowdot from that output (used to isolate the backward from forward
+    rounding); otherwise both are recomputed here in fp64.
+    """
+    s = scores(q, k, scale, causal)
+    if lse is None:
+        lse = logsumexp_rows(s)
+    p = np.exp(s - lse[:, None])
+    if o is None:
+        o = p @ v
+    dv = p.T @ do
+    dp = do @ v.T
+    D = (p * dp).sum(axis=1)
+    D_rowdot = (do * o).sum(axis=1)
+    ds = p * (dp - D[:, None])
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return {"dq": dq, "dk": dk, "dv": dv, "D": D, "D_rowdot": D_rowdot, "dS": ds, "P": p}
+
+
+def forward(q, k, v, scale: float, causal: bool):
+    """Full forward over [B, Hq, Nq, d] / [B, Hkv, Nkv, d].  Returns (O, L) in fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Nq, d = q.shape
+    Hkv = k.shape[1]
+    o = np.zeros((B, Hq, Nq, d))
+    lse = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            hk = kv_head(h, Hq, Hkv)
+            o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, hk], v[b, hk], scale, causal)
+    return o, lse
+
+
+def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=None):
+    """Full backward.  Returns dict of fp64 arrays dq, dk, dv, D, D_rowdot.
+
+    ``groups``: optional iterable of (b, h_kv) pairs; when given only those
+    groups are computed (their query heads' dq/D and the group's dk/dv), the
+    rest of the outputs are NaN.  Used for sampled parity at full size.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    lse = None if lse is None else _f64(lse)
+    o = None if o is None else _f64(o)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    fill = np.nan if groups is not None else 0.0
+    dq = np.full((B, Hq, Nq, d), fill)
+    dk = np.full((B, Hkv, Nkv, d), fill)
+    dv = np.full((B, Hkv, Nkv, d), fill)
+    D = np.full((B, Hq, Nq), fill)
+    D_rowdot = np.full((B, Hq, Nq), fill)
+    todo = groups if groups is not None else [(b, g) for b in range(B) for g in range(Hkv)]
+    for b, g in todo:
+        dk[b, g] = 0.0
+        dv[b, g] = 0.0
+        for h in range(g * G, (g + 1) * G):
+            r = head_backward(q[b, h], k[b, g], v[b, g], do[b, h], scale, causal,
+                              None if lse is None else lse[b, h],
+                              None if o is None else o[b, h])
+            dq[b, h] = r["dq"]
+            dk[b, g] += r["dk"]
+            dv[b, g] += r["dv"]
+            D[b, h] = r["D"]
+            D_rowdot[b, h] = r["D_rowdot"]
+    return {"dq": dq, "dk": dk, "dv": dv, "D": D, "D_rowdot": D_rowdot}
+
+
+def backward_flops(B, Hq, Nq, Nkv, d, causal) -> float:
+    """FLOPs counted for the backward: 10 * B * Hq * Nq * Nkv * d, halved when causal."""
+    f = 10.0 * B * Hq * Nq * Nkv * d
+    return f / 2 if causal else f
