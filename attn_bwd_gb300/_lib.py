@@ -1,0 +1,130 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+Every function here has the name and argument order of its C counterpart.
+Pointer arguments accept an integer device address, ``None`` (NULL) or any
+object with ``data_ptr()`` (a torch tensor); ``stream`` accepts an integer
+handle, ``None`` (the legacy default stream) or a ``torch.cuda.Stream``.
+All arithmetic runs in the CUDA library: if it is not built, loading fails
+loudly -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn_bwd_gb300.so")
+
+FA_OK = 0
+FA_ERR_NULL = 1
+FA_ERR_SHAPE = 2
+FA_ERR_HEADDIM = 3
+FA_ERR_GQA = 4
+FA_ERR_ALIGN = 5
+FA_ERR_WORKSPACE = 6
+FA_ERR_DTYPE = 7
+FA_ERR_CUDA = 8
+FA_ERR_DEVICE_TIMEOUT = 9
+FA_ERR_ARG = 10
+FA_F16 = 0
+FA_BF16 = 1
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+
+_SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_bwd_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
+    "fa_strerror": (ctypes.c_char_p, [_I]),
+    "fa_last_device_error": (_I, [_P]),
+    "fa_selftest_wait_timeout": (_I, [_I, _P]),
+}
+
+_lib = None
+
+
+def load():
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {LIB_PATH} is missing "
+                "(run `python -m attn_bwd_gb300.build` or __graft_entry__.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+def fa_strerror(status: int) -> str:
+    return load().fa_strerror(int(status)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, stream=None) -> int:
+    return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nkv, d,
+                         float(scale), int(causal), int(dtype), _stream(stream))
+
+
+def fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, deterministic) -> int:
+    return load().fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, int(deterministic))
+
+
+def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic,
+           workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                         B, Hq, Hkv, Nq, Nkv, d, float(scale), int(causal), int(dtype), int(deterministic),
+                         _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, Nq, Nkv, d, dtype, deterministic, workspace, workspace_bytes,
+                      stream=None) -> int:
+    return load().fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(lse), B, Hq, Hkv, Nq, Nkv, d, int(dtype),
+                                    int(deterministic), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_main(q, k, v, dO, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic, workspace,
+                workspace_bytes, stream=None) -> int:
+    return load().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nkv, d,
+                              float(scale), int(causal), int(dtype), int(deterministic), _ptr(workspace),
+                              int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_dq(q, k, v, dO, dq, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic, workspace,
+              workspace_bytes, stream=None) -> int:
+    return load().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), B, Hq, Hkv, Nq, Nkv, d, float(scale),
+                            int(causal), int(dtype), int(deterministic), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
+
+
+def fa_last_device_error(stream=None) -> int:
+    return load().fa_last_device_error(_stream(stream))
+
+
+def fa_selftest_wait_timeout(timeout_us, stream=None) -> int:
+    return load().fa_selftest_wait_timeout(int(timeout_us), _stream(stream))

@@ -1,0 +1,169 @@
+// bwd_aux.cu -- the HBM-bound kernels around the backward's main kernel.
+//
+// preprocess: D_i = sum_c dO_ic O_ic per query row in fp32 (the row-wise dot
+//   product of flash_attention_backward.cu, rustytorch rtx-flash-attention,
+//   block "Compute row-wise dot product: dO * O"; the D / delta input of the
+//   Triton kernel in triton #1806), computed once per row instead of once per
+//   CTA.  Fused with it: L*log2(e) per row (the main kernel evaluates
+//   exp(S - L) as exp2(S*scale*log2e - L*log2e)), +inf / 0 on the padding rows
+//   so that padded query rows contribute exactly zero, and the zeroing of the
+//   fp32 dQ accumulator (triton #1806 allocates it zero-filled).
+// convert: dQ = scale * accumulator, rounded once to the 16-bit dtype.
+// Both stream contiguous rows with 16-byte loads and stores; grids are sized
+// in multiples of the SM count and walk the rows with a grid stride.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kSMs = 152;
+
+template <bool BF16>
+__device__ __forceinline__ void widen8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = unpack2<BF16>(w[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// One query row is handled by D/8 consecutive lanes (16 bytes of O and of dO each).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
+                  float* __restrict__ Lg, float* __restrict__ Dv, float4* __restrict__ dq_acc,
+                  long long rows, int Nq, int NqPad) {
+  constexpr int TPR = D / 8;                 // lanes per row
+  constexpr int RPB = 256 / TPR;             // rows per block per sweep
+  const int sub = threadIdx.x % TPR;
+  // The sweep base is block-uniform so every lane reaches the row shuffle below.
+  for (long long base = static_cast<long long>(blockIdx.x) * RPB; base < rows;
+       base += static_cast<long long>(gridDim.x) * RPB) {
+    const long long row = base + threadIdx.x / TPR;
+    const bool valid = row < rows;
+    const long long bh = row / NqPad;
+    const int r = static_cast<int>(row - bh * NqPad);
+    float acc = 0.f;
+    if (valid && r < Nq) {
+      const long long src = (bh * Nq + r) * TPR + sub;
+      float a[8], g[8];
+      widen8<BF16>(__ldg(o + src), a);
+      widen8<BF16>(__ldg(dO + src), g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(a[i], g[i], acc);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+    if (!valid) continue;
+    if (sub == 0) {
+      Dv[row] = acc;
+      Lg[row] = (r < Nq) ? lse[bh * Nq + r] * 1.4426950408889634f : __int_as_float(0x7f800000);
+    }
+    if (dq_acc != nullptr) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq_acc[row * (D / 4) + 2 * sub] = z;
+      dq_acc[row * (D / 4) + 2 * sub + 1] = z;
+    }
+  }
+}
+
+// Each thread converts 8 consecutive fp32 of one row to 16-bit.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, int Nq, int NqPad,
+                  float scale) {
+  constexpr int C8 = D / 8;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n8;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = idx / C8;            // row of dq: bh * Nq + r
+    const int c8 = static_cast<int>(idx - row * C8);
+    const long long bh = row / Nq;
+    const long long r = row - bh * Nq;
+    const long long src = ((bh * NqPad + r) * D) / 4 + 2 * c8;
+    const float4 a = __ldcs(acc + src);
+    const float4 b = __ldcs(acc + src + 1);
+    uint4 out;
+    out.x = pack2<BF16>(a.x * scale, a.y * scale);
+    out.y = pack2<BF16>(a.z * scale, a.w * scale);
+    out.z = pack2<BF16>(b.x * scale, b.y * scale);
+    out.w = pack2<BF16>(b.z * scale, b.w * scale);
+    dq[idx] = out;
+  }
+}
+
+// Waits on a barrier nobody arrives on, bounded by timeout_ns; records the
+// timeout in the status word and exits.
+__global__ void wait_selftest_kernel(unsigned int* status, long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (mbar_try_wait(b, 0)) break;  // never completes: nothing arrives
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(timeout_ns)) {
+        atomicCAS(status, 0u, (kStatusTimeout << 16) | 99u);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+long long grid_for(long long work_items, int per_block) {
+  long long g = (work_items + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(kSMs) * 16;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : g;
+}
+
+template <int D, bool BF16>
+cudaError_t pre_t(const Problem& pb, const void* o, const void* dO, const float* lse, const Workspace& ws,
+                  cudaStream_t stream) {
+  const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.NqPad;
+  const long long grid = grid_for(rows, 256 / (D / 8));
+  preprocess_kernel<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws.Lg, ws.Dv,
+      pb.deterministic ? nullptr : reinterpret_cast<float4*>(ws.dq_acc), rows, pb.Nq, pb.NqPad);
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t conv_t(const Problem& pb, const Workspace& ws, void* dq, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(pb.B) * pb.Hq * pb.Nq * (D / 8);
+  const long long grid = grid_for(n8, 256);
+  dq_convert_kernel<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(ws.dq_acc), static_cast<uint4*>(dq), n8, pb.Nq, pb.NqPad, pb.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, const float* lse,
+                              const Workspace& ws, cudaStream_t stream) {
+  if (pb.d == 128) return pb.bf16 ? pre_t<128, true>(pb, o, dO, lse, ws, stream) : pre_t<128, false>(pb, o, dO, lse, ws, stream);
+  return pb.bf16 ? pre_t<64, true>(pb, o, dO, lse, ws, stream) : pre_t<64, false>(pb, o, dO, lse, ws, stream);
+}
+
+cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, cudaStream_t stream) {
+  if (pb.d == 128) return pb.bf16 ? conv_t<128, true>(pb, ws, dq, stream) : conv_t<128, false>(pb, ws, dq, stream);
+  return pb.bf16 ? conv_t<64, true>(pb, ws, dq, stream) : conv_t<64, false>(pb, ws, dq, stream);
+}
+
+cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,480 @@
+// bwd_main.cu -- KV-tile-parallel attention backward on tcgen05 tensor cores.
+//
+// Decomposition: the sequence-parallel scheme of "Extra transposes cause 8x
+// speedup for sequence-parallel Flash Attention backward" (triton #1806,
+// "Minimal Repro"): one program per (batch, head, KV block) keeps its K and V
+// block resident, walks every query block, accumulates dK and dV on chip and
+// stores them once, while dQ contributions are added into an fp32 buffer.
+// Here one CTA owns a 128-row KV tile of one key/value head and walks the
+// query tiles of every query head of its GQA group ("[Kernel] Flash attention
+// 2", Liger-Kernel #275, "Details"), so dK/dV are reduced over the group on
+// chip.  The per-tile arithmetic is that of flash_attention_backward.cu
+// (rustytorch rtx-flash-attention): recompute S, P = exp(S - L), dV += P^T dO,
+// dP = dO V^T, dS = P o (dP - D), dK += dS^T Q, dQ += dS K.
+//
+// sm_103a mapping (BN = 128 KV rows on the TMEM lanes, BM = 64 query rows):
+//   G1  S^T [BN x BM]  = K  . Q^T      A = K  (smem, K-major), B = Q  (K-major)
+//   G2  dP^T[BN x BM]  = V  . dO^T     A = V  (smem, K-major), B = dO (K-major)
+//   G3  dV  [BN x d ] += P^T . dO      A = P^T  (TMEM, 16-bit), B = dO (MN-major)
+//   G4  dK  [BN x d ] += dS^T . Q      A = dS^T (TMEM, 16-bit), B = Q  (MN-major)
+//   G5  dQ^T[d  x BM]  = K^T . dS^T    A = K  (smem, MN-major), B = dS^T (smem, MN-major)
+// Every operand is read in place from the TMA-written tiles through
+// descriptors of the right major-ness: no transposed copies exist.  That is
+// the lesson of triton #1806, where the orientation of the dQ product alone
+// made an 8x difference.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: K, V once; Q, dO, L, D tiles through a 2-stage ring
+//   warp 1      owns TMEM; one lane issues every tcgen05.mma
+//   warps 4-7   "softmax" group: thread r owns KV row r (TMEM lane r); P, dS
+//   warps 8-11  dQ group: TMEM -> smem fp32 tile -> bulk reduce-add into the
+//               workspace accumulator (skipped in deterministic mode)
+//   epilogue    warps 4-7 write dK (x scale), warps 8-11 write dV
+#include <cstdint>
+#include <climits>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BN = 128;       // KV rows per CTA (TMEM lanes)
+constexpr int BM = 64;        // query rows per tile
+constexpr int STAGES = 2;     // Q/dO ring depth
+constexpr int kThreads = 384;
+
+template <int D>
+struct Layout {
+  static constexpr int NH = D / 64;               // 64-column halves of a row
+  static constexpr int KHALF = BN * 128;          // bytes of one half of a K/V tile
+  static constexpr int QHALF = BM * 128;          // bytes of one half of a Q/dO tile
+  static constexpr int KV_BYTES = NH * KHALF;
+  static constexpr int Q_BYTES = NH * QHALF;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;
+  static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
+  static constexpr int OFF_DS = OFF_DO + STAGES * Q_BYTES;
+  static constexpr int DS_BYTES = BN * BM * 2;    // dS^T, 128 rows x 128 B
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
+  static constexpr int STG_BYTES = BM * D * 4;    // one fp32 dQ tile
+  static constexpr int OFF_LD = OFF_STG + 2 * STG_BYTES;
+  static constexpr int LD_BYTES = 2 * BM * 4;     // L*log2e and D of one tile
+  static constexpr int OFF_BAR = OFF_LD + STAGES * LD_BYTES;
+  static constexpr int NBAR = 20;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int TOTAL = OFF_MISC + 16;
+  static constexpr int ALLOC = TOTAL + 1024;      // slack for 1024-byte alignment
+  // TMEM columns (fp32 accumulators; 16-bit P/dS overwrite the first half of S/dP)
+  static constexpr int COL_DK = 0;
+  static constexpr int COL_DV = D;
+  static constexpr int COL_S = 2 * D;
+  static constexpr int COL_DP = 2 * D + BM;
+  static constexpr int COL_DQ = 2 * D + 2 * BM;
+  static_assert(COL_DQ + BM <= 512, "TMEM budget");
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+// barrier indices
+enum : int {
+  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_DP, B_P, B_DS,
+  B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_STGREADY, B_STGFREE = B_STGREADY + 2, B_END = B_STGFREE + 2
+};
+static_assert(B_END <= 20, "barrier count");
+
+struct Params {
+  const float* Lg;
+  const float* Dv;
+  float* dq_acc;
+  void* dk;
+  void* dv;
+  unsigned int* status;
+  int B, Hq, Hkv, Nq, Nkv, NqPad;
+  float scale, scale_log2;
+  int causal;
+};
+
+// Bounded wait that ignores the abort flag: used only to drain work already
+// in flight before the CTA releases TMEM and exits.
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&pk)[16]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+template <int D, bool BF16, bool DET>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const Params p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  // ---- work item: KV tile j of key/value head hkv of batch b (tile-major order,
+  // so that under causal masking the longest CTAs are scheduled first)
+  const int groups = p.B * p.Hkv;
+  const int j = blockIdx.x / groups;
+  const int gi = blockIdx.x - j * groups;
+  const int b = gi / p.Hkv;
+  const int hkv = gi - b * p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int kv0 = j * BN;
+  const int nQt = (p.Nq + BM - 1) / BM;
+  const int i0 = p.causal ? min(kv0 / BM, nQt) : 0;   // first query tile that sees this KV tile
+  const int per_head = nQt - i0;
+  const int T = G * per_head;                          // tiles this CTA processes
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_KV), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(B_QFULL + s), 1);
+      mbar_init(bar(B_QEMPTY + s), 1);
+    }
+    mbar_init(bar(B_S), 1);
+    mbar_init(bar(B_DP), 1);
+    mbar_init(bar(B_P), 128);
+    mbar_init(bar(B_DS), 128);
+    mbar_init(bar(B_DQFULL), 1);
+    mbar_init(bar(B_DQEMPTY), 128);
+    mbar_init(bar(B_DSFREE), 1);
+    mbar_init(bar(B_ACC), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_STGREADY + s), 128);
+      mbar_init(bar(B_STGFREE + s), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{p.status, abort_flag};
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0 && T > 0) {
+      const int kvh = b * p.Hkv + hkv;
+      mbar_arrive_expect_tx(bar(B_KV), 2 * L::KV_BYTES);
+#pragma unroll
+      for (int hh = 0; hh < L::NH; ++hh) {
+        tma_load_3d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(B_KV), 64 * hh, kv0, kvh);
+        tma_load_3d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(B_KV), 64 * hh, kv0, kvh);
+      }
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % STAGES;
+        const uint32_t ph = (t / STAGES) & 1;
+        if (t >= STAGES && !mbar_wait(bar(B_QEMPTY + s), ph ^ 1, wc, 1)) break;
+        const int h = hkv * G + t / per_head;
+        const int q0 = (i0 + t % per_head) * BM;
+        const int bh = b * p.Hq + h;
+        const uint32_t fb = bar(B_QFULL + s);
+        mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + L::LD_BYTES);
+#pragma unroll
+        for (int hh = 0; hh < L::NH; ++hh) {
+          tma_load_3d(sb + L::OFF_Q + s * L::Q_BYTES + hh * L::QHALF, &tm_q, fb, 64 * hh, q0, bh);
+          tma_load_3d(sb + L::OFF_DO + s * L::Q_BYTES + hh * L::QHALF, &tm_do, fb, 64 * hh, q0, bh);
+        }
+        const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
+        bulk_load(sb + L::OFF_LD + s * L::LD_BYTES, p.Lg + row, BM * 4, fb);
+        bulk_load(sb + L::OFF_LD + s * L::LD_BYTES + BM * 4, p.Dv + row, BM * 4, fb);
+        issued = t + 1;
+      }
+      // Never leave a copy in flight into shared memory this CTA is about to release.
+      drain_wait(bar(B_KV), 0);
+      for (int t = max(0, issued - STAGES); t < issued; ++t)
+        drain_wait(bar(B_QFULL + t % STAGES), (t / STAGES) & 1);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t ID_S = make_idesc_f16(128, BM, BF16, false, false);
+      constexpr uint32_t ID_KV = make_idesc_f16(128, D, BF16, false, true);
+      constexpr uint32_t ID_Q = make_idesc_f16(128, BM, BF16, true, true);
+      const uint32_t tS = tmem + L::COL_S, tdP = tmem + L::COL_DP;
+      const uint32_t tdK = tmem + L::COL_DK, tdV = tmem + L::COL_DV, tdQ = tmem + L::COL_DQ;
+      const uint32_t aK = sb + L::OFF_K, aV = sb + L::OFF_V;
+      bool ok = mbar_wait(bar(B_KV), 0, wc, 2);
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % STAGES;
+        const uint32_t ph = (t / STAGES) & 1;
+        if (!mbar_wait(bar(B_QFULL + s), ph, wc, 3)) break;
+        tc_fence_after();
+        const uint32_t aQ = sb + L::OFF_Q + s * L::Q_BYTES;
+        const uint32_t aO = sb + L::OFF_DO + s * L::Q_BYTES;
+        // G1: S^T = K Q^T  (contraction over d, 16 per instruction)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ok_ = (ks >> 2) * L::KHALF + (ks & 3) * 32;
+          const uint32_t oq = (ks >> 2) * L::QHALF + (ks & 3) * 32;
+          umma_ss(tS, sw128_desc(aK + ok_, 16, 1024), sw128_desc(aQ + oq, 16, 1024), ID_S, ks > 0);
+        }
+        umma_commit(bar(B_S));
+        // G2: dP^T = V dO^T
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ok_ = (ks >> 2) * L::KHALF + (ks & 3) * 32;
+          const uint32_t oq = (ks >> 2) * L::QHALF + (ks & 3) * 32;
+          umma_ss(tdP, sw128_desc(aV + ok_, 16, 1024), sw128_desc(aO + oq, 16, 1024), ID_S, ks > 0);
+        }
+        umma_commit(bar(B_DP));
+        // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
+        if (!mbar_wait(bar(B_P), t & 1, wc, 4)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          umma_ts(tdV, tS + ks * 8, sw128_desc(aO + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+        // G4: dK += dS^T Q
+        if (!mbar_wait(bar(B_DS), t & 1, wc, 5)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          umma_ts(tdK, tdP + ks * 8, sw128_desc(aQ + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+        if constexpr (!DET) {
+          // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
+          // (for d = 64 the upper 64 lanes are unused)
+          if (t > 0 && !mbar_wait(bar(B_DQEMPTY), (t - 1) & 1, wc, 6)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ss(tdQ, sw128_desc(aK + ks * 2048, L::KHALF, 1024),
+                    sw128_desc(sb + L::OFF_DS + ks * 2048, L::DS_BYTES, 1024), ID_Q, ks > 0);
+          umma_commit(bar(B_DQFULL));
+          umma_commit(bar(B_DSFREE));
+        }
+        umma_commit(bar(B_QEMPTY + s));
+      }
+      umma_commit(bar(B_ACC));
+      if (*abort_flag) drain_wait(bar(B_ACC), 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ================================================================ softmax / dS group
+    const int r = threadIdx.x - 128;                       // KV row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + L::COL_S;
+    const uint32_t tdP = tmem + lane_off + L::COL_DP;
+    const int kv = kv0 + r;
+    const bool row_ok = kv < p.Nkv;
+    uint8_t* ds_row = smem + L::OFF_DS + r * 128;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % STAGES;
+      const int q0 = (i0 + t % per_head) * BM;
+      const float* Ls = reinterpret_cast<const float*>(smem + L::OFF_LD + s * L::LD_BYTES);
+      const float* Ds = Ls + BM;
+      // columns c < lim are masked: key kv lies after query q0 + c
+      const int lim = p.causal ? (kv - q0) : INT_MIN;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S), t & 1, wc, 7))) break;
+      tc_fence_after();
+      uint32_t pk[BM / 2];
+#pragma unroll
+      for (int ch = 0; ch < BM / 32; ++ch) {
+        uint32_t sr[32];
+        tmem_ld_x32(tS + ch * 32, sr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(Ls + ch * 32 + 4 * c4);
+          const int c = ch * 32 + 4 * c4;
+          float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 0]), p.scale_log2, -l4.x));
+          float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 1]), p.scale_log2, -l4.y));
+          float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 2]), p.scale_log2, -l4.z));
+          float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 3]), p.scale_log2, -l4.w));
+          if (!row_ok || c + 0 < lim) e0 = 0.f;
+          if (!row_ok || c + 1 < lim) e1 = 0.f;
+          if (!row_ok || c + 2 < lim) e2 = 0.f;
+          if (!row_ok || c + 3 < lim) e3 = 0.f;
+          pk[ch * 16 + 2 * c4] = pack2<BF16>(e0, e1);
+          pk[ch * 16 + 2 * c4 + 1] = pack2<BF16>(e2, e3);
+        }
+      }
+      tmem_st_x32(tS, pk);                  // P^T, 16-bit, into the first BM/2 columns of S
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_P));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 8))) break;
+      tc_fence_after();
+      uint32_t dk[BM / 2];
+#pragma unroll
+      for (int ch = 0; ch < BM / 32; ++ch) {
+        uint32_t dr[32];
+        tmem_ld_x32(tdP + ch * 32, dr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + ch * 32 + 4 * c4);
+          const float2 pa = unpack2<BF16>(pk[ch * 16 + 2 * c4]);
+          const float2 pb = unpack2<BF16>(pk[ch * 16 + 2 * c4 + 1]);
+          const float s0 = pa.x * (__uint_as_float(dr[4 * c4 + 0]) - d4.x);
+          const float s1 = pa.y * (__uint_as_float(dr[4 * c4 + 1]) - d4.y);
+          const float s2 = pb.x * (__uint_as_float(dr[4 * c4 + 2]) - d4.z);
+          const float s3 = pb.y * (__uint_as_float(dr[4 * c4 + 3]) - d4.w);
+          dk[ch * 16 + 2 * c4] = pack2<BF16>(s0, s1);
+          dk[ch * 16 + 2 * c4 + 1] = pack2<BF16>(s2, s3);
+        }
+      }
+      tmem_st_x32(tdP, dk);                 // dS^T, 16-bit, into the first BM/2 columns of dP
+      if constexpr (!DET) {
+        // dS^T row r into shared memory for G5: 128 B per row, 16-byte chunk c
+        // stored at chunk position c ^ (r mod 8) (the 128-byte swizzle).
+        if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (t - 1) & 1, wc, 9))) break;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(ds_row + ((c ^ (r & 7)) << 4)) =
+              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        fence_proxy_async_smem();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_DS));
+    }
+  } else if (warp >= 8) {
+    // ================================================================ dQ group
+    if constexpr (!DET) {
+      const int r = threadIdx.x - 256;                     // TMEM lane == column of dQ
+      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t tdQ = tmem + lane_off + L::COL_DQ;
+      float* stg = reinterpret_cast<float*>(smem + L::OFF_STG);
+      for (int t = 0; t < T; ++t) {
+        const int buf = t & 1;
+        const int use = t >> 1;
+        const int h = hkv * G + t / per_head;
+        const int q0 = (i0 + t % per_head) * BM;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), t & 1, wc, 10))) break;
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld_x32(tdQ, v0);
+        tmem_ld_x32(tdQ + 32, v1);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_DQEMPTY));
+        if (t >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B_STGFREE + buf), (use - 1) & 1, wc, 11))) break;
+        if (r < D) {
+          float* st = stg + buf * (BM * D) + r;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) st[c * D] = __uint_as_float(v0[c]);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) st[(32 + c) * D] = __uint_as_float(v1[c]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_STGREADY + buf));
+        if (r == 0) {
+          if (!mbar_wait(bar(B_STGREADY + buf), use & 1, wc, 12)) {
+            // give up on this tile; the status word already records the failure
+          } else {
+            const size_t row = static_cast<size_t>(b * p.Hq + h) * p.NqPad + q0;
+            bulk_reduce_add_f32(p.dq_acc + row * D, sb + L::OFF_STG + buf * L::STG_BYTES, L::STG_BYTES);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+          }
+          mbar_arrive(bar(B_STGFREE + buf));
+        }
+      }
+      if (r == 0) bulk_wait_group<0>();
+    }
+  }
+
+  // ================================================================ epilogue: dK, dV
+  if (warp >= 4) {
+    const bool is_dk = warp < 8;
+    const int r = threadIdx.x - (is_dk ? 128 : 256);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tacc = tmem + lane_off + (is_dk ? L::COL_DK : L::COL_DV);
+    const int kv = kv0 + r;
+    const float mul = is_dk ? p.scale : 1.0f;
+    uint8_t* out = reinterpret_cast<uint8_t*>(is_dk ? p.dk : p.dv) +
+                   (static_cast<size_t>(b * p.Hkv + hkv) * p.Nkv + kv) * D * 2;
+    bool have = T > 0;
+    if (have) {
+      have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 13));
+      tc_fence_after();
+    }
+    const bool aborted = *abort_flag != 0;
+#pragma unroll 1
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t pk[16];
+      if (have) {
+        uint32_t v[32];
+        tmem_ld_x32(tacc + ch * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack2<BF16>(__uint_as_float(v[2 * c]) * mul, __uint_as_float(v[2 * c + 1]) * mul);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = 0u;
+      }
+      if (kv < p.Nkv && !aborted) store_row_chunk<BF16>(out + ch * 64, pk);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BF16, bool DET>
+cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
+                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  using L = Layout<D>;
+  auto kern = bwd_main_kernel<D, BF16, DET>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  Params p;
+  p.Lg = a.ws.Lg;
+  p.Dv = a.ws.Dv;
+  p.dq_acc = a.ws.dq_acc;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.status = a.status;
+  p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv; p.NqPad = a.pb.NqPad;
+  p.scale = a.pb.scale;
+  p.scale_log2 = a.pb.scale * 1.4426950408889634f;
+  p.causal = a.pb.causal;
+  const long long nkt = (a.pb.Nkv + BN - 1) / BN;
+  const long long grid = nkt * a.pb.B * a.pb.Hkv;
+  kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
+                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  const bool det = a.pb.deterministic != 0;
+  if (a.pb.d == 128) {
+    if (a.pb.bf16) return det ? launch_t<128, true, true>(a, tq, tdo, tk, tv, stream)
+                              : launch_t<128, true, false>(a, tq, tdo, tk, tv, stream);
+    return det ? launch_t<128, false, true>(a, tq, tdo, tk, tv, stream)
+               : launch_t<128, false, false>(a, tq, tdo, tk, tv, stream);
+  }
+  if (a.pb.bf16) return det ? launch_t<64, true, true>(a, tq, tdo, tk, tv, stream)
+                            : launch_t<64, true, false>(a, tq, tdo, tk, tv, stream);
+  return det ? launch_t<64, false, true>(a, tq, tdo, tk, tv, stream)
+             : launch_t<64, false, false>(a, tq, tdo, tk, tv, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,74 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Rows of every per-head query array in the workspace are padded to this.
+constexpr int kRowPad = 128;
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Workspace carve-up shared by every stage of the backward.
+struct Workspace {
+  float* Lg;      // [B*Hq*NqPad]   L * log2(e); +inf on padding rows
+  float* Dv;      // [B*Hq*NqPad]   rowsum(dO o O); 0 on padding rows
+  float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
+};
+
+struct Problem {
+  int B, Hq, Hkv, Nq, Nkv, d;
+  int NqPad;
+  float scale;
+  int causal;
+  int bf16;
+  int deterministic;
+};
+
+struct MainArgs {
+  Problem pb;
+  Workspace ws;
+  void* dk;
+  void* dv;
+  unsigned int* status;
+};
+
+struct DqArgs {
+  Problem pb;
+  Workspace ws;
+  void* dq;
+  unsigned int* status;
+};
+
+struct FwdArgs {
+  Problem pb;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+};
+
+// bwd_aux.cu
+cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, const float* lse,
+                              const Workspace& ws, cudaStream_t stream);
+cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cudaStream_t stream);
+
+// bwd_main.cu: maps are Q, dO (box 64 x 64 rows), K, V (box 64 x 128 rows)
+cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
+                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
+
+// bwd_dq.cu: maps are Q, dO (box 64 x 128 rows), K, V (box 64 x 128 rows)
+cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
+                              const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
+
+// fwd.cu
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,72 @@
+"""torch-tensor front end over the C ABI: checks, output allocation, stream.
+
+PyTorch only supplies device memory and the current stream here; every
+arithmetic step runs in the CUDA library through ``_lib``.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DT = {torch.float16: _lib.FA_F16, torch.bfloat16: _lib.FA_BF16}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_lib.fa_strerror(status)} (fa_status {status})")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != _lib.FA_OK:
+        raise FAError(status, where)
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    return B, Hq, Hkv, Nq, Nkv, d
+
+
+def _need(*ts):
+    for t in ts:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def forward(q, k, v, scale: float, causal: bool, stream=None):
+    """Returns (O, L): O like q, L fp32 [B, Hq, Nq] (natural-log LSE of the scaled scores)."""
+    _need(q, k, v)
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, d, scale, causal, _DT[q.dtype], s), "fa_fwd")
+    return o, lse
+
+
+def workspace(q, k, deterministic: bool) -> torch.Tensor:
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    n = _lib.fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, int(deterministic))
+    if n == 0:
+        raise ValueError("invalid shape for the backward")
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def backward(q, k, v, o, do, lse, scale: float, causal: bool, deterministic: bool = False, ws=None,
+             out=None, stream=None):
+    """Returns (dQ, dK, dV), freshly written (never accumulated)."""
+    _need(q, k, v, o, do, lse)
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    if ws is None:
+        ws = workspace(q, k, deterministic)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, _DT[q.dtype],
+                       int(deterministic), ws, ws.numel(), s), "fa_bwd")
+    return dq, dk, dv

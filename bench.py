@@ -1,0 +1,331 @@
+"""Benchmark of the attention backward on GB300.
+
+One step = one full backward (preprocess, KV-tile-parallel main kernel, dQ
+convert) over the headline workload: B=4, Hq=32, Hkv=8, Nq=Nkv=8192, d=128,
+bf16, causal (the Llama-3-8B shaped sweep of "[Kernel] Flash attention 2",
+Liger-Kernel #275, "Benchmarking", at its 8192 point).  Inputs are seeded
+synthetic N(0,1) tensors resident in HBM; O and L come from this library's
+forward, outside the timed region.  Every input is larger than L2.
+
+Metric: backward TFLOP/s counting 10*B*Hq*Nq*Nkv*d FLOPs, halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--deterministic]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (the
+problem shards by (batch, kv-head) groups with no exchange): weak scaling,
+replicas only, with a barrier and the max over ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention backward TFLOP/s (bf16/fp16) and % of GB300 dense tensor peak"
+PEAKS_FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--n", type=int, default=8192, help="sequence length of the Llama-3 shaped workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload(n):
+    from attn_bwd_gb300 import inputs
+    return inputs.llama_gqa(n)
+
+
+def flops(sh) -> float:
+    f = 10.0 * sh.B * sh.Hq * sh.Nq * sh.Nkv * sh.d
+    return f / 2 if sh.causal else f
+
+
+def config_dict(sh, det, n_gpus):
+    in_bytes = 2 * (2 * sh.B * sh.Hq * sh.Nq * sh.d + 3 * sh.B * sh.Hkv * sh.Nkv * sh.d) + 4 * sh.B * sh.Hq * sh.Nq
+    return {"workload": f"llama3-8b-shaped GQA causal attention backward B={sh.B} Hq={sh.Hq} Hkv={sh.Hkv} "
+                        f"Nq=Nkv={sh.Nq} d={sh.d} {sh.dtype}",
+            "B": sh.B, "Hq": sh.Hq, "Hkv": sh.Hkv, "Nq": sh.Nq, "Nkv": sh.Nkv, "d": sh.d,
+            "causal": sh.causal, "dtype": sh.dtype, "deterministic": det,
+            "inputs": "seeded synthetic N(0,1), O and L from fa_fwd",
+            "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB read per step, L2 = 129 MB)",
+            "parallelism": "replicas" if n_gpus > 1 else "single GPU"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def main_kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("bwd_main.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "attn_bwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(sh, det):
+    """DRAM bytes per main-kernel launch from the committed ncu record, if it still matches the source."""
+    p = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("source_sha") != main_kernel_sha() or bool(rec.get("deterministic")) != det:
+        return None
+    # scale a smaller capture by the tiles processed (traffic grows with the work)
+    return rec["bytes_per_launch"] * flops(sh) / rec["flops_per_launch"]
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = max(float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit())
+        pw = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        loaded = [s for s, p in zip(sm, pw) if p > 300] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def run_cpu_baseline(sh, heads=4):
+    """The fp64 oracle, as it stands, on one (batch, kv-head) group of the workload."""
+    from attn_bwd_gb300 import inputs
+    from oracle import attn_ref
+    G = sh.Hq // sh.Hkv
+    sub = inputs.Shape(1, G, 1, sh.Nq, sh.Nkv, sh.d, sh.causal, sh.dtype)
+    q, k, v, do = inputs.draw(sub, 12345)
+    q, do = q[:, :heads], do[:, :heads]
+    t0 = time.perf_counter()
+    attn_ref.backward(q, k, v, do, sh.softmax_scale, sh.causal)
+    dt = time.perf_counter() - t0
+    f = 10.0 * heads * sh.Nq * sh.Nkv * sh.d / (2 if sh.causal else 1)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} query heads of one (batch, kv-head) group at Nq=Nkv={sh.Nq}, "
+                      f"fp64 numpy/OpenBLAS, {dt:.1f} s wall"}
+
+
+def reference_arm(args):
+    """--impl reference: the fp64 oracle timed on the host cores, one query head per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from attn_bwd_gb300 import inputs
+    from oracle import attn_ref
+    sh = workload(args.n)
+    sub = inputs.Shape(1, 1, 1, sh.Nq, sh.Nkv, sh.d, sh.causal, sh.dtype)
+    q, k, v, do = inputs.draw(sub, 777)
+    f = 10.0 * sh.Nq * sh.Nkv * sh.d / (2 if sh.causal else 1)
+    for _ in range(args.warmup):
+        attn_ref.backward(q, k, v, do, sh.softmax_scale, sh.causal)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        attn_ref.backward(q, k, v, do, sh.softmax_scale, sh.causal)
+    dt = time.perf_counter() - t0
+    val = f * args.steps / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": config_dict(sh, args.deterministic, args.gpus),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one query head per step (B=1, H=1, Nq=Nkv={sh.Nq}, d={sh.d}, causal)"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import torch
+    import torch.distributed as dist
+    from attn_bwd_gb300 import _lib, inputs, torch_api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _lib.load()
+    sh = workload(args.n)
+    det = args.deterministic
+    B, Hq, Hkv, N, d = sh.B, sh.Hq, sh.Hkv, sh.Nq, sh.d
+    dt_code = _lib.FA_BF16 if sh.dtype == "bf16" else _lib.FA_F16
+    q, k, v, do = inputs.draw(sh, 1000 + rank, device=dev)
+    o, lse = torch_api.forward(q, k, v, sh.softmax_scale, sh.causal)
+    ws = torch_api.workspace(q, k, det)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    scale, causal = sh.softmax_scale, int(sh.causal)
+
+    def step(ev=None):
+        st = _lib.fa_bwd_preprocess(o, do, lse, B, Hq, Hkv, N, N, d, dt_code, det, ws, ws.numel(), stream)
+        if ev is not None:
+            ev[0].record(stream)
+        st |= _lib.fa_bwd_main(q, k, v, do, dk, dv, B, Hq, Hkv, N, N, d, scale, causal, dt_code, det, ws,
+                               ws.numel(), stream)
+        if ev is not None:
+            ev[1].record(stream)
+        st |= _lib.fa_bwd_dq(q, k, v, do, dq, B, Hq, Hkv, N, N, d, scale, causal, dt_code, det, ws, ws.numel(),
+                             stream)
+        if st:
+            raise RuntimeError(f"fa_bwd stage failed: {st}")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if _lib.fa_last_device_error(stream) != 0:
+        raise RuntimeError("device status reported a failure during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    main_ms = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    if _lib.fa_last_device_error(stream) != 0:
+        raise RuntimeError("device status reported a failure in the timed region")
+
+    fl = flops(sh)
+    value = world * fl * args.steps / (ms_total * 1e-3) / 1e12
+    peaks, peaks_src = load_peaks()
+    main_avg = sum(main_ms) / len(main_ms)
+    achieved = fl / (main_avg * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = traffic_per_launch(sh, det)
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, lse)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        qq, kk, vv, oo, dd, ll = dev_in
+        st = _lib.fa_bwd(qq, kk, vv, oo, dd, ll, dq, dk, dv, B, Hq, Hkv, N, N, d, scale, causal, dt_code, det, ws,
+                         ws.numel(), stream)
+        if st:
+            raise RuntimeError(f"fa_bwd failed: {st}")
+        for dst, src in zip(host_out, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * fl * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": sh.dtype, "data": "synthetic",
+        "config": config_dict(sh, det, world),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic},
+        "peak_source": f"{peaks_src} bf16 burst (MEASURED_PEAKS.json); main-kernel fraction of the sustained "
+                       f"{peaks.get('bf16_tflops_sustained')} TFLOP/s: {achieved / float(peaks.get('bf16_tflops_sustained', peak)):.3f}",
+        "percent_of_peak": 100.0 * value / peak,
+        "kernel_ms": {"bwd_main_avg": main_avg, "bwd_main_min": min(main_ms),
+                      "other_avg": ms_total / args.steps - main_avg},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(sh)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention backward library.
+ *
+ * What is computed (per batch b and query head h; key/value head
+ * h_kv = h / (Hq / Hkv), consecutive query heads share one key/value head):
+ *
+ *   S = scale * Q K^T, causal: S[i][j] = -inf when j > i  (top-left)
+ *   L = logsumexp_j S       (natural log of the scaled scores)
+ *   P = exp(S - L),  O = P V
+ *   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO o O),  dS = P o (dP - D)
+ *   dQ = scale * dS K,  dK = scale * dS^T Q
+ *   dK, dV of a key/value head are summed over the query heads of its group.
+ *
+ * Sources: "flash_attention_backward.cu" (rustytorch rtx-flash-attention),
+ * kernel flash_attention_backward_kernel, blocks "Recompute attention scores",
+ * "Apply causal mask", "Compute softmax probabilities from scores and LSE",
+ * "Compute dS", "Compute dQ", "Compute dK", "Compute dV" and "Compute row-wise
+ * dot product: dO * O"; the sequence-parallel kernel in "Extra transposes cause
+ * 8x speedup for sequence-parallel Flash Attention backward" (triton #1806,
+ * "Minimal Repro"), which accumulates dQ in an fp32 buffer across KV tiles;
+ * GQA as listed in "[Kernel] Flash attention 2" (Liger-Kernel #275, "Details").
+ *
+ * Layout (all entry points): contiguous row-major tensors
+ *   Q, O, dO, dQ : [B, Hq,  Nq,  d]   16-bit (fp16 or bf16, see fa_dtype)
+ *   K, V, dK, dV : [B, Hkv, Nkv, d]   16-bit
+ *   L (lse)      : [B, Hq,  Nq]       fp32, natural-log LSE of the scaled scores
+ * d must be 64 or 128.  Every pointer is a DEVICE pointer on the current
+ * device, 16-byte aligned.  The caller owns every buffer (inputs, outputs and
+ * workspace) and the stream; the library allocates no device memory, keeps no
+ * state besides one status word per kernel family, and never synchronises
+ * inside fa_fwd / fa_bwd*.  All work is enqueued on `stream`.
+ *
+ * Errors: each call validates its arguments first and, on failure, returns a
+ * non-zero fa_status WITHOUT launching anything.  FA_ERR_CUDA reports a
+ * failed launch (cudaGetLastError).  Device-side waits are bounded: a wait
+ * that runs out sets a status word read by fa_last_device_error().
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,            /* a required pointer is NULL                         */
+  FA_ERR_SHAPE = 2,           /* B, Hq, Hkv, Nq or Nkv < 1, or above the size limit */
+  FA_ERR_HEADDIM = 3,         /* d not in {64, 128}                                 */
+  FA_ERR_GQA = 4,             /* Hq not a multiple of Hkv                           */
+  FA_ERR_ALIGN = 5,           /* a pointer is not 16-byte aligned                   */
+  FA_ERR_WORKSPACE = 6,       /* workspace NULL or smaller than fa_bwd_workspace_size */
+  FA_ERR_DTYPE = 7,           /* dtype not an fa_dtype value                        */
+  FA_ERR_CUDA = 8,            /* a CUDA launch or driver call failed                */
+  FA_ERR_DEVICE_TIMEOUT = 9,  /* a bounded device-side wait ran out (see fa_last_device_error) */
+  FA_ERR_ARG = 10             /* another argument is out of range (scale not finite, ...) */
+} fa_status;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* Largest Nq / Nkv accepted (rows per head). */
+#define FA_MAX_SEQ (1 << 24)
+
+/*
+ * fa_fwd -- exact attention forward: O = softmax(scale Q K^T [+ causal mask]) V
+ * and L = logsumexp of the scaled (masked) scores, natural log.
+ * Source: the forward that produces the O and LSE consumed by the backward in
+ * flash_attention_backward.cu ("Compute softmax probabilities from scores and
+ * LSE"); forward tables in "[Issue]: Backward performance" (ROCm #44).
+ * q,k,v: inputs; o: output [B,Hq,Nq,d] (overwritten); lse: output [B,Hq,Nq] fp32.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
+           int dtype, cudaStream_t stream);
+
+/*
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs.
+ * Holds D = rowsum(dO o O) and L*log2(e) per query row (rows padded to a
+ * multiple of 128), plus, when deterministic == 0, the fp32 dQ accumulator
+ * [B, Hq, Nq padded, d] of the sequence-parallel scheme (triton #1806,
+ * "Minimal Repro": dq is an fp32 buffer that every KV-tile program adds to).
+ * Returns 0 when the shape is invalid.
+ */
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int deterministic);
+
+/*
+ * fa_bwd -- full backward: dq, dk, dv (all OVERWRITTEN, not accumulated).
+ * Runs fa_bwd_preprocess, fa_bwd_main and fa_bwd_dq in order on `stream`.
+ * deterministic == 0: dQ is accumulated with fp32 reductions in the workspace
+ *   (summation order not fixed; results may differ in the last bits between runs).
+ * deterministic != 0: dQ comes from a separate query-tile-parallel pass with a
+ *   fixed summation order; results are bit-identical from run to run.
+ * workspace: device buffer of at least fa_bwd_workspace_size(...) bytes,
+ *   256-byte aligned; its contents on entry do not matter.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv,
+           int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
+           int dtype, int deterministic, void* workspace, size_t workspace_bytes,
+           cudaStream_t stream);
+
+/*
+ * fa_bwd_preprocess -- step 1 of fa_bwd: D_i = sum_c dO_ic O_ic (fp32), the
+ * row-wise dot product the pages precompute (flash_attention_backward.cu,
+ * "Compute row-wise dot product: dO * O"; the D input of the Triton kernel in
+ * triton #1806), L*log2(e) per row, and (deterministic == 0) zeroes the fp32
+ * dQ accumulator.  Writes only the workspace.
+ */
+int fa_bwd_preprocess(const void* o, const void* dO, const float* lse,
+                      int B, int Hq, int Hkv, int Nq, int Nkv, int d, int dtype, int deterministic,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_bwd_main -- step 2 of fa_bwd: the KV-tile-parallel kernel.  One CTA per
+ * (128-row KV tile, key/value head, batch) walks every query tile of every
+ * query head of its GQA group (triton #1806, "Minimal Repro": grid over
+ * (batch, head, KV block), loop over query blocks), recomputes S and P, and
+ * accumulates dV += P^T dO and dK += dS^T Q on the tensor cores; dK, dV are
+ * written once.  With deterministic == 0 it also forms dQ_tile = dS K and adds
+ * it into the workspace accumulator.  Needs fa_bwd_preprocess first.
+ */
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO,
+                void* dk, void* dv,
+                int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
+                int dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+
+/*
+ * fa_bwd_dq -- step 3 of fa_bwd.  deterministic == 0: converts the fp32
+ * accumulator to dq = scale * acc in the 16-bit dtype.  deterministic != 0:
+ * runs the query-tile-parallel pass (flash_attention_backward.cu's
+ * query-block grid with dQ kept on chip, "Compute dQ") and writes dq directly.
+ * Needs fa_bwd_preprocess (and, for deterministic == 0, fa_bwd_main) first.
+ */
+int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+              int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
+              int dtype, int deterministic, void* workspace, size_t workspace_bytes,
+              cudaStream_t stream);
+
+/* Human-readable name of an fa_status value (static string, never NULL). */
+const char* fa_strerror(int status);
+
+/*
+ * fa_last_device_error -- synchronises `stream`, then reads and clears the
+ * device status words.  Returns FA_ERR_DEVICE_TIMEOUT if any bounded wait in
+ * a kernel ran out since the last call, FA_ERR_CUDA if the sync failed,
+ * FA_OK otherwise.
+ */
+int fa_last_device_error(cudaStream_t stream);
+
+/*
+ * fa_selftest_wait_timeout -- launches one CTA that waits on a barrier no one
+ * arrives on, with a wait bound of `timeout_us` microseconds (1..5,000,000).
+ * The kernel gives up, records FA_ERR_DEVICE_TIMEOUT and exits cleanly; the
+ * caller then sees it through fa_last_device_error().  This exercises the
+ * failure-detection path without faulting or hanging the GPU.
+ */
+int fa_selftest_wait_timeout(int timeout_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,111 @@
+"""CPU tests of the C ABI: the library builds, loads, exports every symbol that
+include/fa.h declares, and rejects bad arguments with the documented codes
+before touching the GPU (all calls below fail validation, so no device is needed)."""
+import os
+import re
+
+import pytest
+
+from attn_bwd_gb300 import _lib
+from attn_bwd_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+A = 0x100000       # a fake, 16-byte-aligned "device pointer": never dereferenced
+W = 0x200000       # a fake, 256-byte-aligned workspace
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_last_device_error",
+              "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq", "fa_selftest_wait_timeout"):
+        assert s in syms, s
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"{s} declared in include/fa.h but not exported"
+        assert s in _lib._SIGNATURES, f"{s} has no binding"
+
+
+def test_strerror_covers_all_codes(lib):
+    for code in range(0, 11):
+        assert _lib.fa_strerror(code) != "unknown fa_status"
+    assert _lib.fa_strerror(1234) == "unknown fa_status"
+
+
+def test_workspace_size_formula(lib):
+    # rows padded to 128: L*log2e and D (fp32 each), plus the fp32 dQ accumulator in atomic mode
+    rows = 2 * 4 * 128
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 1) == 2 * rows * 4
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 0) == 2 * rows * 4 + rows * 64 * 4
+    assert _lib.fa_bwd_workspace_size(2, 4, 3, 100, 100, 64, 0) == 0     # GQA mismatch
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 0, 100, 64, 0) == 0       # empty sequence
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 96, 0) == 0     # head dim
+
+
+def _bwd(**kw):
+    args = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=1, Nq=64, Nkv=64, d=64,
+                scale=0.125, causal=0, dtype=_lib.FA_F16, deterministic=0, workspace=W, workspace_bytes=0)
+    args.update(kw)
+    return _lib.fa_bwd(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), _lib.FA_ERR_NULL),
+    (dict(lse=None), _lib.FA_ERR_NULL),
+    (dict(dv=None), _lib.FA_ERR_NULL),
+    (dict(Nq=0), _lib.FA_ERR_SHAPE),
+    (dict(Nkv=-3), _lib.FA_ERR_SHAPE),
+    (dict(B=0), _lib.FA_ERR_SHAPE),
+    (dict(Nq=(1 << 24) + 1), _lib.FA_ERR_SHAPE),
+    (dict(d=96), _lib.FA_ERR_HEADDIM),
+    (dict(d=256), _lib.FA_ERR_HEADDIM),
+    (dict(Hq=3, Hkv=2), _lib.FA_ERR_GQA),
+    (dict(dtype=7), _lib.FA_ERR_DTYPE),
+    (dict(q=A + 8), _lib.FA_ERR_ALIGN),
+    (dict(dk=A + 2), _lib.FA_ERR_ALIGN),
+    (dict(workspace=None), _lib.FA_ERR_WORKSPACE),
+    (dict(workspace=W + 16, workspace_bytes=1 << 30), _lib.FA_ERR_ALIGN),
+    (dict(workspace_bytes=100), _lib.FA_ERR_WORKSPACE),
+    (dict(scale=float("nan"), workspace_bytes=1 << 30), _lib.FA_ERR_ARG),
+    (dict(scale=float("inf"), workspace_bytes=1 << 30), _lib.FA_ERR_ARG),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_deterministic_workspace_is_smaller(lib):
+    need_det = _lib.fa_bwd_workspace_size(1, 2, 1, 64, 64, 64, 1)
+    need_atomic = _lib.fa_bwd_workspace_size(1, 2, 1, 64, 64, 64, 0)
+    assert need_det < need_atomic
+    # a deterministic-size workspace is too small for atomic mode
+    assert _bwd(deterministic=0, workspace_bytes=need_det) == _lib.FA_ERR_WORKSPACE
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    f = _lib.fa_fwd
+    assert f(None, A, A, A, A, 1, 2, 1, 8, 8, 64, 0.1, 0, 0) == _lib.FA_ERR_NULL
+    assert f(A, A, A, A, A, 1, 2, 1, 8, 8, 32, 0.1, 0, 0) == _lib.FA_ERR_HEADDIM
+    assert f(A, A, A, A, A, 1, 3, 2, 8, 8, 64, 0.1, 0, 0) == _lib.FA_ERR_GQA
+    assert f(A, A, A, A, A + 4, 1, 2, 1, 8, 8, 64, 0.1, 0, 0) == _lib.FA_ERR_ALIGN
+    assert f(A, A, A, A, A, 1, 2, 1, 8, 8, 64, 0.1, 0, 2) == _lib.FA_ERR_DTYPE
+
+
+def test_stage_entry_points_validate(lib):
+    assert _lib.fa_bwd_preprocess(None, A, A, 1, 2, 1, 8, 8, 64, 0, 0, W, 1 << 30) == _lib.FA_ERR_NULL
+    assert _lib.fa_bwd_main(A, A, A, A, A, A, 1, 2, 1, 8, 8, 64, 0.1, 0, 0, 0, W, 16) == _lib.FA_ERR_WORKSPACE
+    assert _lib.fa_bwd_dq(A, A, A, A, None, 1, 2, 1, 8, 8, 64, 0.1, 0, 0, 1, W, 1 << 30) == _lib.FA_ERR_NULL
+    assert _lib.fa_selftest_wait_timeout(0) == _lib.FA_ERR_ARG
+    assert _lib.fa_selftest_wait_timeout(10_000_000) == _lib.FA_ERR_ARG

@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs.
+
+Tolerance (per tensor): max|gpu - ref| <= 1e-2 * max|ref| + 1e-3, for O and L
+of the forward and dQ, dK, dV of the backward.  The backward consumes the
+GPU forward's 16-bit O and fp32 L; the oracle recomputes everything in fp64
+from the 16-bit inputs, so the bound covers both passes' rounding.
+
+Sizes: every workload in full where the oracle finishes in seconds; the
+Llama-3 shaped sweep at N >= 2048 is checked on sampled (batch, kv-head)
+groups, in the launch configuration the benchmark times (the whole problem
+runs on the GPU; the oracle computes the sampled groups exactly).
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from attn_bwd_gb300 import _lib, inputs, torch_api
+from oracle import attn_ref
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-2, 1e-3
+
+
+def _np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def errors(pairs):
+    """pairs: name -> (gpu array, ref array). Returns (failures, report)."""
+    fails, lines = [], []
+    for name, (got, ref) in pairs.items():
+        mask = ~np.isnan(ref)
+        err = float(np.abs(got[mask] - ref[mask]).max()) if mask.any() else 0.0
+        bound = REL * float(np.abs(ref[mask]).max()) + ABS if mask.any() else ABS
+        ok = err <= bound and np.isfinite(got[mask]).all()
+        lines.append(f"{name}: max|err|={err:.3e} bound={bound:.3e} {'ok' if ok else 'FAIL'}")
+        if not ok:
+            fails.append(name)
+    return fails, "\n".join(lines)
+
+
+@functools.lru_cache(maxsize=8)
+def oracle_full(shape: inputs.Shape, seed: int):
+    q, k, v, do = inputs.draw(shape, seed)
+    o, lse = attn_ref.forward(q, k, v, shape.softmax_scale, shape.causal)
+    g = attn_ref.backward(q, k, v, do, shape.softmax_scale, shape.causal)
+    return (q, k, v, do), o, lse, g
+
+
+def gpu_run(q, k, v, do, shape, deterministic):
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = torch_api.forward(qd, kd, vd, shape.softmax_scale, shape.causal)
+    dq, dk, dv = torch_api.backward(qd, kd, vd, o, dod, lse, shape.softmax_scale, shape.causal, deterministic)
+    torch.cuda.synchronize()
+    assert _lib.fa_last_device_error() == _lib.FA_OK
+    return o, lse, dq, dk, dv
+
+
+def check_full(shape, seed, deterministic):
+    (q, k, v, do), o_ref, lse_ref, g = oracle_full(shape, seed)
+    o, lse, dq, dk, dv = gpu_run(q, k, v, do, shape, deterministic)
+    fails, rep = errors({"O": (_np(o), o_ref), "L": (_np(lse), lse_ref),
+                         "dQ": (_np(dq), g["dq"]), "dK": (_np(dk), g["dk"]), "dV": (_np(dv), g["dv"])})
+    assert not fails, f"{shape.name()} det={deterministic}\n{rep}"
+
+
+# ---------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("det", [False, True])
+def test_tiny_mha(det):
+    check_full(inputs.tiny_mha()[0], 1, det)
+
+
+@pytest.mark.parametrize("det", [False, True])
+@pytest.mark.parametrize("shape", inputs.ragged(), ids=lambda s: s.name())
+def test_ragged(shape, det):
+    check_full(shape, 2, det)
+
+
+@pytest.mark.parametrize("shape", inputs.mid_sweep(), ids=lambda s: s.name())
+def test_mid_sweep(shape):
+    check_full(shape, 3, False)
+
+
+@pytest.mark.parametrize("shape", [s for s in inputs.mid_sweep() if s.d == 128 and s.Nq == 784],
+                         ids=lambda s: s.name())
+def test_mid_sweep_deterministic(shape):
+    check_full(shape, 3, True)
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_long_uniform(det):
+    check_full(inputs.long_uniform()[0], 4, det)
+
+
+@pytest.mark.parametrize("n", [32, 64, 128, 256, 512, 1024])
+def test_llama_gqa_full(n):
+    check_full(inputs.llama_gqa(n), 5, False)
+
+
+@pytest.mark.parametrize("n", [96, 1000])
+def test_llama_gqa_full_deterministic(n):
+    check_full(inputs.llama_gqa(n), 5, True)
+
+
+@pytest.mark.parametrize("n", [2048, 4096, 8192, 16384])
+def test_llama_gqa_sampled(n):
+    """Full-size run on the GPU; the oracle computes two (batch, kv-head) groups exactly."""
+    shape = inputs.llama_gqa(n)
+    q, k, v, do = inputs.draw(shape, 5, device="cuda")
+    o, lse, dq, dk, dv = gpu_run(q, k, v, do, shape, False)
+    G = shape.Hq // shape.Hkv
+    groups = [(0, 0), (shape.B - 1, shape.Hkv - 1)]
+    pairs = {}
+    for b, g in groups:
+        hs = slice(g * G, (g + 1) * G)
+        sl = lambda t, h: t[b:b + 1, h].cpu()  # noqa: E731
+        qs, dos = sl(q, hs), sl(do, hs)
+        ks, vs = sl(k, slice(g, g + 1)), sl(v, slice(g, g + 1))
+        o_ref, lse_ref = attn_ref.forward(qs, ks, vs, shape.softmax_scale, True)
+        r = attn_ref.backward(qs, ks, vs, dos, shape.softmax_scale, True)
+        pairs[f"O[{b},{g}]"] = (_np(o[b:b + 1, hs]), o_ref)
+        pairs[f"L[{b},{g}]"] = (_np(lse[b:b + 1, hs]), lse_ref)
+        pairs[f"dQ[{b},{g}]"] = (_np(dq[b:b + 1, hs]), r["dq"])
+        pairs[f"dK[{b},{g}]"] = (_np(dk[b:b + 1, g:g + 1]), r["dk"])
+        pairs[f"dV[{b},{g}]"] = (_np(dv[b:b + 1, g:g + 1]), r["dv"])
+    fails, rep = errors(pairs)
+    assert not fails, rep
+    # a property that holds on every head: sum over keys of dK is exactly zero
+    col = dk.float().sum(dim=2).abs().max().item()
+    assert col <= 1e-2 * dk.float().abs().max().item() * shape.Nkv ** 0.5, col
+
+
+# ------------------------------------------------------------ extra shapes
+
+@pytest.mark.parametrize("det", [False, True])
+@pytest.mark.parametrize("shape", [
+    inputs.Shape(1, 4, 2, 77, 200, 64, True, "bf16"),      # Nq < Nkv, top-left causal
+    inputs.Shape(1, 4, 2, 300, 130, 128, True, "f16"),     # Nq > Nkv
+    inputs.Shape(2, 6, 3, 129, 257, 128, False, "bf16"),   # one past a tile on both sides
+    inputs.Shape(1, 8, 1, 64, 64, 64, True, "bf16"),       # 8 query heads share one kv head
+], ids=lambda s: s.name())
+def test_extra_shapes(shape, det):
+    check_full(shape, 6, det)
+
+
+# ------------------------------------------------------------ step-level checks
+
+def test_preprocess_rowdot_and_padding():
+    """Step 1 alone: D = rowsum(dO o O) from the given O, L*log2(e), and padding rows."""
+    shape = inputs.Shape(2, 3, 3, 100, 100, 128, False, "bf16")
+    q, k, v, do = (t.cuda() for t in inputs.draw(shape, 7))
+    o, lse = torch_api.forward(q, k, v, shape.softmax_scale, False)
+    ws = torch_api.workspace(q, k, False)
+    ws.fill_(0xFF)
+    st = _lib.fa_bwd_preprocess(o, do, lse, 2, 3, 3, 100, 100, 128, _lib.FA_BF16, 0, ws, ws.numel(),
+                                torch.cuda.current_stream())
+    assert st == 0
+    torch.cuda.synchronize()
+    rows = 2 * 3 * 128
+    f = ws.view(torch.float32)
+    Lg = f[:rows].view(2, 3, 128).cpu().double().numpy()
+    Dv = f[rows:2 * rows].view(2, 3, 128).cpu().double().numpy()
+    acc = f[2 * rows:2 * rows + rows * 128]
+    D_ref = (_np(o) * _np(do)).sum(-1)
+    np.testing.assert_allclose(Dv[:, :, :100], D_ref, rtol=1e-5, atol=1e-5)
+    assert (Dv[:, :, 100:] == 0).all()
+    np.testing.assert_allclose(Lg[:, :, :100], _np(lse) * np.log2(np.e), rtol=1e-6, atol=1e-6)
+    assert np.isinf(Lg[:, :, 100:]).all() and (Lg[:, :, 100:] > 0).all()
+    assert (acc == 0).all()
+
+
+def test_deterministic_is_bitwise_reproducible():
+    shape = inputs.llama_gqa(1000)
+    q, k, v, do = (t.cuda() for t in inputs.draw(shape, 8))
+    o, lse = torch_api.forward(q, k, v, shape.softmax_scale, True)
+    a = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, True)
+    b = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, True)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_atomic_mode_dk_dv_are_reproducible():
+    """dK, dV never go through atomics, so they are bitwise stable in either mode."""
+    shape = inputs.Shape(2, 8, 2, 700, 700, 128, True, "bf16")
+    q, k, v, do = (t.cuda() for t in inputs.draw(shape, 9))
+    o, lse = torch_api.forward(q, k, v, shape.softmax_scale, True)
+    a = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, False)
+    b = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2 * b[0].float().abs().max().item() + 1e-3
+
+
+def test_outputs_are_overwritten_not_accumulated():
+    shape = inputs.Shape(1, 2, 1, 150, 150, 64, True, "f16")
+    q, k, v, do = (t.cuda() for t in inputs.draw(shape, 10))
+    o, lse = torch_api.forward(q, k, v, shape.softmax_scale, True)
+    ref = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, False)
+    out = tuple(torch.full_like(t, 7.0) for t in ref)
+    got = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, False, out=out)
+    torch.cuda.synchronize()
+    for x, y in zip(ref, got):
+        assert (x.float() - y.float()).abs().max().item() <= 1e-2 * x.float().abs().max().item() + 1e-3
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection without a fault: a wait nobody satisfies gives up and reports."""
+    s = torch.cuda.current_stream()
+    assert _lib.fa_last_device_error(s) == _lib.FA_OK
+    assert _lib.fa_selftest_wait_timeout(20000, s) == _lib.FA_OK
+    assert _lib.fa_last_device_error(s) == _lib.FA_ERR_DEVICE_TIMEOUT
+    assert _lib.fa_last_device_error(s) == _lib.FA_OK        # read-and-clear
+    check_full(inputs.tiny_mha()[0], 1, False)              # the context still works
