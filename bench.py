@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--deterministic", action="store_true")
@@ -86,7 +86,7 @@ def main_kernel_sha() -> str:
 
 def traffic_per_launch(sh, det):
     """DRAM bytes per main-kernel launch from the committed ncu record, if it still matches the source."""
-    p = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
+    p = os.path.join(ROOT, "profiles", "bwd_main_traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -112,7 +112,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
