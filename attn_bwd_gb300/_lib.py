@@ -44,7 +44,10 @@ _SIGNATURES = {
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_last_device_error": (_I, [_P]),
     "fa_selftest_wait_timeout": (_I, [_I, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
 }
+
+FA_STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -128,3 +131,12 @@ def fa_last_device_error(stream=None) -> int:
 
 def fa_selftest_wait_timeout(timeout_us, stream=None) -> int:
     return load().fa_selftest_wait_timeout(int(timeout_us), _stream(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic,
+                   stream=None) -> int:
+    """fa_bwd without a workspace argument, for callers that cannot allocate device memory
+    (its scratch is a fixed FA_STATIC_SCRATCH_BYTES array inside the library)."""
+    return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, Hq, Hkv, Nq, Nkv, d, float(scale), int(causal), int(dtype),
+                                 int(deterministic), _stream(stream))

@@ -140,6 +140,35 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void*
               int dtype, int deterministic, void* workspace, size_t workspace_bytes,
               cudaStream_t stream);
 
+/* Size of the scratch array compiled into the library for fa_bwd_noalloc (64 MiB per GPU). */
+#define FA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers of
+ * this library that have no way to obtain a workspace: for example a plugin
+ * inside an inference engine whose host framework owns every device
+ * allocation and offers no scratch, or a serving loop that forbids cudaMalloc
+ * after start-up because it synchronises the device and fragments the pool.
+ * Same arguments and results as fa_bwd, minus the workspace: the scratch is a
+ * fixed array of FA_STATIC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ * Limit: returns FA_ERR_WORKSPACE, launching nothing, when
+ * fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, deterministic) exceeds
+ * FA_STATIC_SCRATCH_BYTES (deterministic mode needs 8 bytes per query row,
+ * rows padded to 128 per head; atomic mode 8 + 4*d bytes per padded row).
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the one array, and each call rewrites
+ * everything it reads from it, so earlier contents never matter; but calls
+ * that overlap on the GPU (unordered streams or host threads) race on it.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
+                   int dtype, int deterministic, cudaStream_t stream);
+
 /* Human-readable name of an fa_status value (static string, never NULL). */
 const char* fa_strerror(int status);
 
