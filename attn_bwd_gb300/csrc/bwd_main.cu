@@ -23,13 +23,25 @@
 // the lesson of triton #1806, where the orientation of the dQ product alone
 // made an 8x difference.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer: K, V once; Q, dO, L, D tiles through a 2-stage ring
-//   warp 1      owns TMEM; one lane issues every tcgen05.mma
-//   warps 4-7   "softmax" group: thread r owns KV row r (TMEM lane r); P, dS
-//   warps 8-11  dQ group: TMEM -> smem fp32 tile -> bulk reduce-add into the
-//               workspace accumulator (skipped in deterministic mode)
-//   epilogue    warps 4-7 write dK (x scale), warps 8-11 write dV
+// Warp roles (512 threads):
+//   warp 0       TMA producer: K, V once; Q, dO, L, D tiles through a 4-stage ring
+//   warp 1       owns TMEM; one lane issues every tcgen05.mma
+//   warps 4-11   two "softmax" groups: thread r of group w owns KV row r (TMEM
+//                lane r) and query columns [32w, 32w+32) of each tile; P, dS
+//   warps 12-15  dQ group: TMEM -> registers -> red.global.add.f32 into the
+//                workspace accumulator, one 128-byte row segment per warp
+//                instruction (idle in deterministic mode)
+//   epilogue     group 0 writes dK (x scale), group 1 writes dV
+//
+// Schedule.  S^T is double-buffered in TMEM and computed two tiles ahead:
+//   G1(0) G2(0) G1(1) | per t: [P(t)] G3(t) [dS(t)] G4(t) G5(t) G2(t+1) G1(t+2)
+// where [x] waits for the softmax groups.  When the softmax groups finish
+// dS(t), S^T(t+1) is already in TMEM, so they go straight on to P(t+1) while
+// the tensor core runs G4/G5 of tile t.  The MMA unit executes one CTA's
+// tcgen05.mma instructions in issue order, which is what lets G1(t+2) reuse
+// the S^T buffer that G3(t) read, and G2(t+1) overwrite the dS^T that G4(t)
+// read, without further waits.  The ring keeps Q/dO loads about two tiles
+// ahead of their first use (a load under full load takes ~1 us).
 #include <cstdint>
 #include <climits>
 
@@ -41,8 +53,8 @@ namespace {
 
 constexpr int BN = 128;       // KV rows per CTA (TMEM lanes)
 constexpr int BM = 64;        // query rows per tile
-constexpr int STAGES = 2;     // Q/dO ring depth
-constexpr int kThreads = 384;
+constexpr int STAGES = 4;     // Q/dO ring depth: loads run ~2 tiles ahead of use
+constexpr int kThreads = 512;
 
 template <int D>
 struct Layout {
@@ -57,29 +69,30 @@ struct Layout {
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_BYTES;
   static constexpr int DS_BYTES = BN * BM * 2;    // dS^T, 128 rows x 128 B
-  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
-  static constexpr int STG_BYTES = BM * D * 4;    // one fp32 dQ tile
-  static constexpr int OFF_LD = OFF_STG + 2 * STG_BYTES;
+  static constexpr int OFF_LD = OFF_DS + DS_BYTES;
   static constexpr int LD_BYTES = 2 * BM * 4;     // L*log2e and D of one tile
   static constexpr int OFF_BAR = OFF_LD + STAGES * LD_BYTES;
   static constexpr int NBAR = 20;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = TOTAL + 1024;      // slack for 1024-byte alignment
-  // TMEM columns (fp32 accumulators; 16-bit P/dS overwrite the first half of S/dP)
+  // TMEM columns (fp32 accumulators).  Two S^T buffers; the 16-bit P^T (dS^T)
+  // of query columns [32w, 32w+32) is packed into columns [32w, 32w+16) of the
+  // S^T (dP^T) buffer, i.e. into the half its own softmax group already read.
   static constexpr int COL_DK = 0;
   static constexpr int COL_DV = D;
-  static constexpr int COL_S = 2 * D;
-  static constexpr int COL_DP = 2 * D + BM;
-  static constexpr int COL_DQ = 2 * D + 2 * BM;
+  static constexpr int COL_S = 2 * D;               // buffers at COL_S and COL_S + BM
+  static constexpr int COL_DP = 2 * D + 2 * BM;
+  static constexpr int COL_DQ = 2 * D + 3 * BM;
   static_assert(COL_DQ + BM <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 // barrier indices
+// (S and P have one barrier per S^T buffer: tile t uses buffer t & 1)
 enum : int {
-  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_DP, B_P, B_DS,
-  B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_STGREADY, B_STGFREE = B_STGREADY + 2, B_END = B_STGFREE + 2
+  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_DP = B_P + 2, B_DS,
+  B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_END
 };
 static_assert(B_END <= 20, "barrier count");
 
@@ -126,8 +139,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
-  // ---- work item: KV tile j of key/value head hkv of batch b (tile-major order,
-  // so that under causal masking the longest CTAs are scheduled first)
+  // ---- work item: KV tile j of key/value head hkv of batch b, tile-major, so
+  // that under causal masking the longest CTAs (small j) are scheduled first.
+  // (A (batch, kv-head)-major order, tried for L2 reuse, measured slower.)
   const int groups = p.B * p.Hkv;
   const int j = blockIdx.x / groups;
   const int gi = blockIdx.x - j * groups;
@@ -146,18 +160,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), 1);
     }
-    mbar_init(bar(B_S), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_S + i), 1);
+      mbar_init(bar(B_P + i), 256);
+    }
     mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_P), 128);
-    mbar_init(bar(B_DS), 128);
+    mbar_init(bar(B_DS), 256);
     mbar_init(bar(B_DQFULL), 1);
     mbar_init(bar(B_DQEMPTY), 128);
     mbar_init(bar(B_DSFREE), 1);
     mbar_init(bar(B_ACC), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_STGREADY + s), 128);
-      mbar_init(bar(B_STGFREE + s), 1);
-    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -212,26 +224,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t ID_S = make_idesc_f16(128, BM, BF16, false, false);
       constexpr uint32_t ID_KV = make_idesc_f16(128, D, BF16, false, true);
       constexpr uint32_t ID_Q = make_idesc_f16(128, BM, BF16, true, true);
-      const uint32_t tS = tmem + L::COL_S, tdP = tmem + L::COL_DP;
+      const uint32_t tdP = tmem + L::COL_DP;
       const uint32_t tdK = tmem + L::COL_DK, tdV = tmem + L::COL_DV, tdQ = tmem + L::COL_DQ;
       const uint32_t aK = sb + L::OFF_K, aV = sb + L::OFF_V;
-      bool ok = mbar_wait(bar(B_KV), 0, wc, 2);
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % STAGES;
-        const uint32_t ph = (t / STAGES) & 1;
-        if (!mbar_wait(bar(B_QFULL + s), ph, wc, 3)) break;
-        tc_fence_after();
-        const uint32_t aQ = sb + L::OFF_Q + s * L::Q_BYTES;
-        const uint32_t aO = sb + L::OFF_DO + s * L::Q_BYTES;
-        // G1: S^T = K Q^T  (contraction over d, 16 per instruction)
+      auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BM; };
+      auto q_tile = [&](int t) -> uint32_t { return sb + L::OFF_Q + (t % STAGES) * L::Q_BYTES; };
+      auto do_tile = [&](int t) -> uint32_t { return sb + L::OFF_DO + (t % STAGES) * L::Q_BYTES; };
+      // G1: S^T = K Q^T  (contraction over d, 16 per instruction)
+      auto issue_g1 = [&](int t) {
+        const uint32_t aQ = q_tile(t), tS = s_buf(t);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ok_ = (ks >> 2) * L::KHALF + (ks & 3) * 32;
           const uint32_t oq = (ks >> 2) * L::QHALF + (ks & 3) * 32;
           umma_ss(tS, sw128_desc(aK + ok_, 16, 1024), sw128_desc(aQ + oq, 16, 1024), ID_S, ks > 0);
         }
-        umma_commit(bar(B_S));
-        // G2: dP^T = V dO^T
+        umma_commit(bar(B_S + (t & 1)));
+      };
+      // G2: dP^T = V dO^T
+      auto issue_g2 = [&](int t) {
+        const uint32_t aO = do_tile(t);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ok_ = (ks >> 2) * L::KHALF + (ks & 3) * 32;
@@ -239,18 +251,41 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           umma_ss(tdP, sw128_desc(aV + ok_, 16, 1024), sw128_desc(aO + oq, 16, 1024), ID_S, ks > 0);
         }
         umma_commit(bar(B_DP));
-        // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
-        if (!mbar_wait(bar(B_P), t & 1, wc, 4)) break;
+      };
+      // 16-bit A operand column for query rows [16ks, 16ks+16): group ks/2, second half if ks odd
+      auto a_col = [](int ks) -> uint32_t { return static_cast<uint32_t>(32 * (ks >> 1) + 8 * (ks & 1)); };
+
+      bool ok = mbar_wait(bar(B_KV), 0, wc, 2) && mbar_wait(bar(B_QFULL), 0, wc, 3);
+      if (ok) {
         tc_fence_after();
+        issue_g1(0);
+        issue_g2(0);
+        if (T > 1) {
+          ok = mbar_wait(bar(B_QFULL + 1), 0, wc, 3);
+          tc_fence_after();
+          if (ok) issue_g1(1);
+        }
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % STAGES;
+        // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
+        if (!mbar_wait(bar(B_P + (t & 1)), (t >> 1) & 1, wc, 4)) break;
+        tc_fence_after();
+        {
+          const uint32_t tS = s_buf(t), aO = do_tile(t);
 #pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks)
-          umma_ts(tdV, tS + ks * 8, sw128_desc(aO + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+          for (int ks = 0; ks < BM / 16; ++ks)
+            umma_ts(tdV, tS + a_col(ks), sw128_desc(aO + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+        }
         // G4: dK += dS^T Q
         if (!mbar_wait(bar(B_DS), t & 1, wc, 5)) break;
         tc_fence_after();
+        {
+          const uint32_t aQ = q_tile(t);
 #pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks)
-          umma_ts(tdK, tdP + ks * 8, sw128_desc(aQ + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+          for (int ks = 0; ks < BM / 16; ++ks)
+            umma_ts(tdK, tdP + a_col(ks), sw128_desc(aQ + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+        }
         if constexpr (!DET) {
           // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
           // (for d = 64 the upper 64 lanes are unused)
@@ -264,38 +299,46 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           umma_commit(bar(B_DSFREE));
         }
         umma_commit(bar(B_QEMPTY + s));
+        // dP^T of the next tile (overwrites dS^T(t), which G4 above has been issued to read),
+        // then S^T two tiles ahead into the buffer P^T(t) occupied (G3 above reads it first)
+        if (t + 1 < T) issue_g2(t + 1);
+        if (t + 2 < T) {
+          if (!mbar_wait(bar(B_QFULL + (t + 2) % STAGES), ((t + 2) / STAGES) & 1, wc, 3)) break;
+          tc_fence_after();
+          issue_g1(t + 2);
+        }
       }
       umma_commit(bar(B_ACC));
       if (*abort_flag) drain_wait(bar(B_ACC), 0);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ================================================================ softmax / dS group
-    const int r = threadIdx.x - 128;                       // KV row == TMEM lane
+  } else if (warp >= 4 && warp < 12) {
+    // ================================================================ softmax / dS groups
+    const int grp = (warp - 4) >> 2;                      // query columns [32 grp, 32 grp + 32)
+    const int r = threadIdx.x - 128 - 128 * grp;          // KV row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + L::COL_S;
-    const uint32_t tdP = tmem + lane_off + L::COL_DP;
+    const uint32_t tdP = tmem + lane_off + L::COL_DP + 32 * grp;
     const int kv = kv0 + r;
     const bool row_ok = kv < p.Nkv;
     uint8_t* ds_row = smem + L::OFF_DS + r * 128;
     for (int t = 0; t < T; ++t) {
       const int s = t % STAGES;
       const int q0 = (i0 + t % per_head) * BM;
-      const float* Ls = reinterpret_cast<const float*>(smem + L::OFF_LD + s * L::LD_BYTES);
+      const float* Ls = reinterpret_cast<const float*>(smem + L::OFF_LD + s * L::LD_BYTES) + 32 * grp;
       const float* Ds = Ls + BM;
-      // columns c < lim are masked: key kv lies after query q0 + c
-      const int lim = p.causal ? (kv - q0) : INT_MIN;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S), t & 1, wc, 7))) break;
+      const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BM + 32 * grp;
+      // columns c < lim are masked: key kv lies after query q0 + 32 grp + c
+      const int lim = p.causal ? (kv - q0 - 32 * grp) : INT_MIN;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 7))) break;
       tc_fence_after();
-      uint32_t pk[BM / 2];
-#pragma unroll
-      for (int ch = 0; ch < BM / 32; ++ch) {
+      uint32_t pk[16];
+      {
         uint32_t sr[32];
-        tmem_ld_x32(tS + ch * 32, sr);
+        tmem_ld_x32(tS, sr);
         tmem_ld_wait();
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(Ls + ch * 32 + 4 * c4);
-          const int c = ch * 32 + 4 * c4;
+          const float4 l4 = *reinterpret_cast<const float4*>(Ls + 4 * c4);
+          const int c = 4 * c4;
           float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 0]), p.scale_log2, -l4.x));
           float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 1]), p.scale_log2, -l4.y));
           float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 2]), p.scale_log2, -l4.z));
@@ -304,60 +347,59 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (!row_ok || c + 1 < lim) e1 = 0.f;
           if (!row_ok || c + 2 < lim) e2 = 0.f;
           if (!row_ok || c + 3 < lim) e3 = 0.f;
-          pk[ch * 16 + 2 * c4] = pack2<BF16>(e0, e1);
-          pk[ch * 16 + 2 * c4 + 1] = pack2<BF16>(e2, e3);
+          pk[2 * c4] = pack2<BF16>(e0, e1);
+          pk[2 * c4 + 1] = pack2<BF16>(e2, e3);
         }
       }
-      tmem_st_x32(tS, pk);                  // P^T, 16-bit, into the first BM/2 columns of S
+      tmem_st_x16(tS, pk);                  // P^T, 16-bit, over the columns just read
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_P));
+      mbar_arrive(bar(B_P + (t & 1)));
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 8))) break;
       tc_fence_after();
-      uint32_t dk[BM / 2];
-#pragma unroll
-      for (int ch = 0; ch < BM / 32; ++ch) {
+      uint32_t dk[16];
+      {
         uint32_t dr[32];
-        tmem_ld_x32(tdP + ch * 32, dr);
+        tmem_ld_x32(tdP, dr);
         tmem_ld_wait();
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(Ds + ch * 32 + 4 * c4);
-          const float2 pa = unpack2<BF16>(pk[ch * 16 + 2 * c4]);
-          const float2 pb = unpack2<BF16>(pk[ch * 16 + 2 * c4 + 1]);
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + 4 * c4);
+          const float2 pa = unpack2<BF16>(pk[2 * c4]);
+          const float2 pb = unpack2<BF16>(pk[2 * c4 + 1]);
           const float s0 = pa.x * (__uint_as_float(dr[4 * c4 + 0]) - d4.x);
           const float s1 = pa.y * (__uint_as_float(dr[4 * c4 + 1]) - d4.y);
           const float s2 = pb.x * (__uint_as_float(dr[4 * c4 + 2]) - d4.z);
           const float s3 = pb.y * (__uint_as_float(dr[4 * c4 + 3]) - d4.w);
-          dk[ch * 16 + 2 * c4] = pack2<BF16>(s0, s1);
-          dk[ch * 16 + 2 * c4 + 1] = pack2<BF16>(s2, s3);
+          dk[2 * c4] = pack2<BF16>(s0, s1);
+          dk[2 * c4 + 1] = pack2<BF16>(s2, s3);
         }
       }
-      tmem_st_x32(tdP, dk);                 // dS^T, 16-bit, into the first BM/2 columns of dP
+      tmem_st_x16(tdP, dk);                 // dS^T, 16-bit, over the columns just read
       if constexpr (!DET) {
-        // dS^T row r into shared memory for G5: 128 B per row, 16-byte chunk c
-        // stored at chunk position c ^ (r mod 8) (the 128-byte swizzle).
+        // dS^T row r into shared memory for G5: 128 B per row (this group's
+        // 64 B are 16-byte chunks 4 grp .. 4 grp + 3), chunk c stored at chunk
+        // position c ^ (r mod 8) (the 128-byte swizzle).
         if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (t - 1) & 1, wc, 9))) break;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int i = 0; i < 4; ++i) {
+          const int c = 4 * grp + i;
           *reinterpret_cast<uint4*>(ds_row + ((c ^ (r & 7)) << 4)) =
-              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+              make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+        }
         fence_proxy_async_smem();
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_DS));
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ================================================================ dQ group
     if constexpr (!DET) {
-      const int r = threadIdx.x - 256;                     // TMEM lane == column of dQ
+      const int r = threadIdx.x - 384;                     // TMEM lane == column of dQ
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tdQ = tmem + lane_off + L::COL_DQ;
-      float* stg = reinterpret_cast<float*>(smem + L::OFF_STG);
       for (int t = 0; t < T; ++t) {
-        const int buf = t & 1;
-        const int use = t >> 1;
         const int h = hkv * G + t / per_head;
         const int q0 = (i0 + t % per_head) * BM;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), t & 1, wc, 10))) break;
@@ -368,34 +410,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(bar(B_DQEMPTY));
-        if (t >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B_STGFREE + buf), (use - 1) & 1, wc, 11))) break;
+        // Thread r holds column r of the 64 x d tile: for each query row, the 32
+        // lanes of a warp add one contiguous 128-byte segment of the accumulator.
         if (r < D) {
-          float* st = stg + buf * (BM * D) + r;
+          float* dst = p.dq_acc + (static_cast<size_t>(b * p.Hq + h) * p.NqPad + q0) * D + r;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) st[c * D] = __uint_as_float(v0[c]);
+          for (int c = 0; c < 32; ++c) red_add_f32(dst + c * D, __uint_as_float(v0[c]));
 #pragma unroll
-          for (int c = 0; c < 32; ++c) st[(32 + c) * D] = __uint_as_float(v1[c]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(B_STGREADY + buf));
-        if (r == 0) {
-          if (!mbar_wait(bar(B_STGREADY + buf), use & 1, wc, 12)) {
-            // give up on this tile; the status word already records the failure
-          } else {
-            const size_t row = static_cast<size_t>(b * p.Hq + h) * p.NqPad + q0;
-            bulk_reduce_add_f32(p.dq_acc + row * D, sb + L::OFF_STG + buf * L::STG_BYTES, L::STG_BYTES);
-            bulk_commit_group();
-            bulk_wait_group_read<0>();
-          }
-          mbar_arrive(bar(B_STGFREE + buf));
+          for (int c = 0; c < 32; ++c) red_add_f32(dst + (32 + c) * D, __uint_as_float(v1[c]));
         }
       }
-      if (r == 0) bulk_wait_group<0>();
     }
   }
 
   // ================================================================ epilogue: dK, dV
-  if (warp >= 4) {
+  if (warp >= 4 && warp < 12) {
     const bool is_dk = warp < 8;
     const int r = threadIdx.x - (is_dk ? 128 : 256);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
