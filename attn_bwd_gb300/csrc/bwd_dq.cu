@@ -152,7 +152,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       constexpr uint32_t ID_S = make_idesc_f16(128, BK, BF16, false, false);
       constexpr uint32_t ID_Q = make_idesc_f16(128, D, BF16, false, true);
       const uint32_t tS = tmem + L::COL_S, tdP = tmem + L::COL_DP, tdQ = tmem + L::COL_DQ;
-      const uint32_t aQ = sb + L::OFF_Q, aO = sb + L::OFF_DO;
+      const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q, 16, 1024), dO_k = sw128_desc(sb + L::OFF_DO, 16, 1024);
       bool ok = mbar_wait(bar(B_Q), 0, wc, 22);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % STAGES;
@@ -161,16 +161,19 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tc_fence_after();
         const uint32_t aK = sb + L::OFF_KV + s * 2 * L::TILE;
         const uint32_t aV = aK + L::TILE;
+        // descriptors built once per tile, stepped by compile-time offsets >> 4
+        const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aV, 16, 1024);
+        const uint64_t dK_mn = sw128_desc(aK, L::HALF, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t o = (ks >> 2) * L::HALF + (ks & 3) * 32;
-          umma_ss(tS, sw128_desc(aQ + o, 16, 1024), sw128_desc(aK + o, 16, 1024), ID_S, ks > 0);
+          const uint64_t o = static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
+          umma_ss(tS, dQ_k + o, dK_k + o, ID_S, ks > 0);
         }
         umma_commit(bar(B_S));
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t o = (ks >> 2) * L::HALF + (ks & 3) * 32;
-          umma_ss(tdP, sw128_desc(aO + o, 16, 1024), sw128_desc(aV + o, 16, 1024), ID_S, ks > 0);
+          const uint64_t o = static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
+          umma_ss(tdP, dO_k + o, dV_k + o, ID_S, ks > 0);
         }
         umma_commit(bar(B_DP));
         if (!mbar_wait(bar(B_DS), t & 1, wc, 24)) break;
@@ -178,7 +181,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // dQ += dS K: dS (16-bit) in the first BK/2 columns of S, K read MN-major
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks)
-          umma_ts(tdQ, tS + ks * 8, sw128_desc(aK + ks * 2048, L::HALF, 1024), ID_Q, (t > 0 || ks > 0));
+          umma_ts(tdQ, tS + ks * 8, dK_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_Q, (t > 0 || ks > 0));
         umma_commit(bar(B_KVEMPTY + s));
       }
       umma_commit(bar(B_ACC));

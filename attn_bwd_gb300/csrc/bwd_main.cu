@@ -16,7 +16,7 @@
 //   G1  S^T [BN x BM]  = K  . Q^T      A = K  (smem, K-major), B = Q  (K-major)
 //   G2  dP^T[BN x BM]  = V  . dO^T     A = V  (smem, K-major), B = dO (K-major)
 //   G3  dV  [BN x d ] += P^T . dO      A = P^T  (TMEM, 16-bit), B = dO (MN-major)
-//   G4  dK  [BN x d ] += dS^T . Q      A = dS^T (TMEM, 16-bit), B = Q  (MN-major)
+//   G4  dK  [BN x d ] += dS^T . Q      A = dS^T (smem, K-major), B = Q  (MN-major)
 //   G5  dQ^T[d  x BM]  = K^T . dS^T    A = K  (smem, MN-major), B = dS^T (smem, MN-major)
 // Every operand is read in place from the TMA-written tiles through
 // descriptors of the right major-ness: no transposed copies exist.  That is
@@ -34,14 +34,16 @@
 //   epilogue     group 0 writes dK (x scale), group 1 writes dV
 //
 // Schedule.  S^T is double-buffered in TMEM and computed two tiles ahead:
-//   G1(0) G2(0) G1(1) | per t: [P(t)] G3(t) [dS(t)] G4(t) G5(t) G2(t+1) G1(t+2)
+//   G1(0) G2(0) G1(1) | per t: [P(t)] G3(t) G1(t+2) [dP(t) loaded] G2(t+1) [dS(t)] G4(t) G5(t)
 // where [x] waits for the softmax groups.  When the softmax groups finish
 // dS(t), S^T(t+1) is already in TMEM, so they go straight on to P(t+1) while
-// the tensor core runs G4/G5 of tile t.  The MMA unit executes one CTA's
-// tcgen05.mma instructions in issue order, which is what lets G1(t+2) reuse
-// the S^T buffer that G3(t) read, and G2(t+1) overwrite the dS^T that G4(t)
-// read, without further waits.  The ring keeps Q/dO loads about two tiles
-// ahead of their first use (a load under full load takes ~1 us).
+// the tensor core runs G4/G5 of tile t.  dS^T goes only to shared memory, so
+// the single dP^T buffer is free as soon as the softmax groups have loaded it
+// and G2(t+1) overlaps their dS(t) arithmetic.  The MMA unit executes one
+// CTA's tcgen05.mma instructions in issue order, which is what lets G1(t+2)
+// reuse the S^T buffer that G3(t) read without a further wait.  The ring keeps
+// Q/dO loads about two tiles ahead of their first use (a load under full load
+// takes ~1 us).
 #include <cstdint>
 #include <climits>
 
@@ -76,9 +78,9 @@ struct Layout {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = TOTAL + 1024;      // slack for 1024-byte alignment
-  // TMEM columns (fp32 accumulators).  Two S^T buffers; the 16-bit P^T (dS^T)
-  // of query columns [32w, 32w+32) is packed into columns [32w, 32w+16) of the
-  // S^T (dP^T) buffer, i.e. into the half its own softmax group already read.
+  // TMEM columns (fp32 accumulators).  Two S^T buffers; the 16-bit P^T of
+  // query columns [32w, 32w+32) is packed into columns [32w, 32w+16) of its
+  // S^T buffer, i.e. into the half its own softmax group already read.
   static constexpr int COL_DK = 0;
   static constexpr int COL_DV = D;
   static constexpr int COL_S = 2 * D;               // buffers at COL_S and COL_S + BM
@@ -91,7 +93,7 @@ struct Layout {
 // barrier indices
 // (S and P have one barrier per S^T buffer: tile t uses buffer t & 1)
 enum : int {
-  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_DP = B_P + 2, B_DS,
+  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_DP = B_P + 2, B_DPFREE, B_DS,
   B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_END
 };
 static_assert(B_END <= 20, "barrier count");
@@ -165,6 +167,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(bar(B_P + i), 256);
     }
     mbar_init(bar(B_DP), 1);
+    mbar_init(bar(B_DPFREE), 256);
     mbar_init(bar(B_DS), 256);
     mbar_init(bar(B_DQFULL), 1);
     mbar_init(bar(B_DQEMPTY), 128);
@@ -222,7 +225,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ================================================================ MMA issuer
     if (lane == 0 && T > 0) {
       constexpr uint32_t ID_S = make_idesc_f16(128, BM, BF16, false, false);
-      constexpr uint32_t ID_KV = make_idesc_f16(128, D, BF16, false, true);
+      constexpr uint32_t ID_KV = make_idesc_f16(128, D, BF16, false, true);   // A K-major (TMEM or smem), B MN-major
       constexpr uint32_t ID_Q = make_idesc_f16(128, BM, BF16, true, true);
       const uint32_t tdP = tmem + L::COL_DP;
       const uint32_t tdK = tmem + L::COL_DK, tdV = tmem + L::COL_DV, tdQ = tmem + L::COL_DQ;
@@ -230,26 +233,35 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BM; };
       auto q_tile = [&](int t) -> uint32_t { return sb + L::OFF_Q + (t % STAGES) * L::Q_BYTES; };
       auto do_tile = [&](int t) -> uint32_t { return sb + L::OFF_DO + (t % STAGES) * L::Q_BYTES; };
+      // One thread issues every MMA, so per-instruction work is kept minimal:
+      // each operand tile's descriptor is built once and stepped by
+      // compile-time offsets (the start address is the descriptor's low field,
+      // so adding offset >> 4 advances it).
+      const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aV, 16, 1024);
+      const uint64_t dK_mn = sw128_desc(aK, L::KHALF, 1024);
+      const uint64_t dS_mn = sw128_desc(sb + L::OFF_DS, L::DS_BYTES, 1024);
+      const uint64_t dS_k = sw128_desc(sb + L::OFF_DS, 16, 1024);
+      // K-major step ks (16 elements of d): 64-column half ks/4, 32 bytes per step inside it
+      auto kstep = [](int ks, int half_bytes) -> uint64_t {
+        return static_cast<uint64_t>(((ks >> 2) * half_bytes + (ks & 3) * 32) >> 4);
+      };
+      // MN-major step ks: 16 rows of 128 bytes
+      auto mnstep = [](int ks) -> uint64_t { return static_cast<uint64_t>((ks * 2048) >> 4); };
       // G1: S^T = K Q^T  (contraction over d, 16 per instruction)
       auto issue_g1 = [&](int t) {
-        const uint32_t aQ = q_tile(t), tS = s_buf(t);
+        const uint64_t dQ_k = sw128_desc(q_tile(t), 16, 1024);
+        const uint32_t tS = s_buf(t);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ok_ = (ks >> 2) * L::KHALF + (ks & 3) * 32;
-          const uint32_t oq = (ks >> 2) * L::QHALF + (ks & 3) * 32;
-          umma_ss(tS, sw128_desc(aK + ok_, 16, 1024), sw128_desc(aQ + oq, 16, 1024), ID_S, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(tS, dK_k + kstep(ks, L::KHALF), dQ_k + kstep(ks, L::QHALF), ID_S, ks > 0);
         umma_commit(bar(B_S + (t & 1)));
       };
       // G2: dP^T = V dO^T
       auto issue_g2 = [&](int t) {
-        const uint32_t aO = do_tile(t);
+        const uint64_t dO_k = sw128_desc(do_tile(t), 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ok_ = (ks >> 2) * L::KHALF + (ks & 3) * 32;
-          const uint32_t oq = (ks >> 2) * L::QHALF + (ks & 3) * 32;
-          umma_ss(tdP, sw128_desc(aV + ok_, 16, 1024), sw128_desc(aO + oq, 16, 1024), ID_S, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(tdP, dV_k + kstep(ks, L::KHALF), dO_k + kstep(ks, L::QHALF), ID_S, ks > 0);
         umma_commit(bar(B_DP));
       };
       // 16-bit A operand column for query rows [16ks, 16ks+16): group ks/2, second half if ks odd
@@ -272,19 +284,32 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!mbar_wait(bar(B_P + (t & 1)), (t >> 1) & 1, wc, 4)) break;
         tc_fence_after();
         {
-          const uint32_t tS = s_buf(t), aO = do_tile(t);
+          const uint32_t tS = s_buf(t);
+          const uint64_t dO_mn = sw128_desc(do_tile(t), L::QHALF, 1024);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks)
-            umma_ts(tdV, tS + a_col(ks), sw128_desc(aO + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+            umma_ts(tdV, tS + a_col(ks), dO_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
         }
-        // G4: dK += dS^T Q
+        // S^T two tiles ahead, into the buffer P^T(t) occupied (G3 above reads it first)
+        if (t + 2 < T) {
+          if (!mbar_wait(bar(B_QFULL + (t + 2) % STAGES), ((t + 2) / STAGES) & 1, wc, 3)) break;
+          tc_fence_after();
+          issue_g1(t + 2);
+        }
+        // dP^T of the next tile as soon as the softmax groups have loaded dP^T(t)
+        if (t + 1 < T) {
+          if (!mbar_wait(bar(B_DPFREE), t & 1, wc, 14)) break;
+          tc_fence_after();
+          issue_g2(t + 1);
+        }
+        // G4: dK += dS^T Q  (dS^T from its smem tile, K-major; contraction over the query rows)
         if (!mbar_wait(bar(B_DS), t & 1, wc, 5)) break;
         tc_fence_after();
         {
-          const uint32_t aQ = q_tile(t);
+          const uint64_t dQ_mn = sw128_desc(q_tile(t), L::QHALF, 1024);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks)
-            umma_ts(tdK, tdP + a_col(ks), sw128_desc(aQ + ks * 2048, L::QHALF, 1024), ID_KV, (t > 0 || ks > 0));
+            umma_ss(tdK, dS_k + static_cast<uint64_t>((ks * 32) >> 4), dQ_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
         }
         if constexpr (!DET) {
           // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
@@ -293,20 +318,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
-            umma_ss(tdQ, sw128_desc(aK + ks * 2048, L::KHALF, 1024),
-                    sw128_desc(sb + L::OFF_DS + ks * 2048, L::DS_BYTES, 1024), ID_Q, ks > 0);
+            umma_ss(tdQ, dK_mn + mnstep(ks), dS_mn + mnstep(ks), ID_Q, ks > 0);
           umma_commit(bar(B_DQFULL));
-          umma_commit(bar(B_DSFREE));
         }
+        umma_commit(bar(B_DSFREE));
         umma_commit(bar(B_QEMPTY + s));
-        // dP^T of the next tile (overwrites dS^T(t), which G4 above has been issued to read),
-        // then S^T two tiles ahead into the buffer P^T(t) occupied (G3 above reads it first)
-        if (t + 1 < T) issue_g2(t + 1);
-        if (t + 2 < T) {
-          if (!mbar_wait(bar(B_QFULL + (t + 2) % STAGES), ((t + 2) / STAGES) & 1, wc, 3)) break;
-          tc_fence_after();
-          issue_g1(t + 2);
-        }
       }
       umma_commit(bar(B_ACC));
       if (*abort_flag) drain_wait(bar(B_ACC), 0);
@@ -362,6 +378,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t dr[32];
         tmem_ld_x32(tdP, dr);
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_DPFREE));         // dP^T buffer may now take the next tile's G2
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = *reinterpret_cast<const float4*>(Ds + 4 * c4);
@@ -375,11 +393,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           dk[2 * c4 + 1] = pack2<BF16>(s2, s3);
         }
       }
-      tmem_st_x16(tdP, dk);                 // dS^T, 16-bit, over the columns just read
-      if constexpr (!DET) {
-        // dS^T row r into shared memory for G5: 128 B per row (this group's
-        // 64 B are 16-byte chunks 4 grp .. 4 grp + 3), chunk c stored at chunk
-        // position c ^ (r mod 8) (the 128-byte swizzle).
+      {
+        // dS^T row r into shared memory, the operand of G4 (K-major A) and G5
+        // (MN-major B): 128 B per row (this group's 64 B are 16-byte chunks
+        // 4 grp .. 4 grp + 3), chunk c stored at chunk position c ^ (r mod 8)
+        // (the 128-byte swizzle).
         if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (t - 1) & 1, wc, 9))) break;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -389,8 +407,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         fence_proxy_async_smem();
       }
-      tmem_st_wait();
-      tc_fence_before();
       mbar_arrive(bar(B_DS));
     }
   } else if (warp >= 12) {
