@@ -148,16 +148,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         drain_wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {   // the whole warp walks the loop; elect.sync issues each MMA
       constexpr uint32_t ID_S = make_idesc_f16(128, BK, BF16, false, false);
       constexpr uint32_t ID_Q = make_idesc_f16(128, D, BF16, false, true);
       const uint32_t tS = tmem + L::COL_S, tdP = tmem + L::COL_DP, tdQ = tmem + L::COL_DQ;
       const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q, 16, 1024), dO_k = sw128_desc(sb + L::OFF_DO, 16, 1024);
-      bool ok = mbar_wait(bar(B_Q), 0, wc, 22);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 22));
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % STAGES;
         const uint32_t ph = (t / STAGES) & 1;
-        if (!mbar_wait(bar(B_KVFULL + s), ph, wc, 23)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_KVFULL + s), ph, wc, 23))) break;
         tc_fence_after();
         const uint32_t aK = sb + L::OFF_KV + s * 2 * L::TILE;
         const uint32_t aV = aK + L::TILE;
@@ -167,24 +167,24 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t o = static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
-          umma_ss(tS, dQ_k + o, dK_k + o, ID_S, ks > 0);
+          umma_ss_warp(tS, dQ_k + o, dK_k + o, ID_S, ks > 0);
         }
-        umma_commit(bar(B_S));
+        umma_commit_warp(bar(B_S));
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t o = static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
-          umma_ss(tdP, dO_k + o, dV_k + o, ID_S, ks > 0);
+          umma_ss_warp(tdP, dO_k + o, dV_k + o, ID_S, ks > 0);
         }
-        umma_commit(bar(B_DP));
-        if (!mbar_wait(bar(B_DS), t & 1, wc, 24)) break;
+        umma_commit_warp(bar(B_DP));
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DS), t & 1, wc, 24))) break;
         tc_fence_after();
         // dQ += dS K: dS (16-bit) in the first BK/2 columns of S, K read MN-major
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks)
-          umma_ts(tdQ, tS + ks * 8, dK_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_Q, (t > 0 || ks > 0));
-        umma_commit(bar(B_KVEMPTY + s));
+          umma_ts_warp(tdQ, tS + ks * 8, dK_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_Q, (t > 0 || ks > 0));
+        umma_commit_warp(bar(B_KVEMPTY + s));
       }
-      umma_commit(bar(B_ACC));
+      umma_commit_warp(bar(B_ACC));
       if (*abort_flag) drain_wait(bar(B_ACC), 0);
     }
   } else if (warp >= 4) {

@@ -223,7 +223,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0 && T > 0) {
+    if (T > 0) {   // the whole warp walks the loop; elect.sync issues each MMA
       constexpr uint32_t ID_S = make_idesc_f16(128, BM, BF16, false, false);
       constexpr uint32_t ID_KV = make_idesc_f16(128, D, BF16, false, true);   // A K-major (TMEM or smem), B MN-major
       constexpr uint32_t ID_Q = make_idesc_f16(128, BM, BF16, true, true);
@@ -253,27 +253,27 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tS = s_buf(t);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          umma_ss(tS, dK_k + kstep(ks, L::KHALF), dQ_k + kstep(ks, L::QHALF), ID_S, ks > 0);
-        umma_commit(bar(B_S + (t & 1)));
+          umma_ss_warp(tS, dK_k + kstep(ks, L::KHALF), dQ_k + kstep(ks, L::QHALF), ID_S, ks > 0);
+        umma_commit_warp(bar(B_S + (t & 1)));
       };
       // G2: dP^T = V dO^T
       auto issue_g2 = [&](int t) {
         const uint64_t dO_k = sw128_desc(do_tile(t), 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          umma_ss(tdP, dV_k + kstep(ks, L::KHALF), dO_k + kstep(ks, L::QHALF), ID_S, ks > 0);
-        umma_commit(bar(B_DP));
+          umma_ss_warp(tdP, dV_k + kstep(ks, L::KHALF), dO_k + kstep(ks, L::QHALF), ID_S, ks > 0);
+        umma_commit_warp(bar(B_DP));
       };
       // 16-bit A operand column for query rows [16ks, 16ks+16): group ks/2, second half if ks odd
       auto a_col = [](int ks) -> uint32_t { return static_cast<uint32_t>(32 * (ks >> 1) + 8 * (ks & 1)); };
 
-      bool ok = mbar_wait(bar(B_KV), 0, wc, 2) && mbar_wait(bar(B_QFULL), 0, wc, 3);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KV), 0, wc, 2)) && __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL), 0, wc, 3));
       if (ok) {
         tc_fence_after();
         issue_g1(0);
         issue_g2(0);
         if (T > 1) {
-          ok = mbar_wait(bar(B_QFULL + 1), 0, wc, 3);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + 1), 0, wc, 3));
           tc_fence_after();
           if (ok) issue_g1(1);
         }
@@ -281,50 +281,50 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % STAGES;
         // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
-        if (!mbar_wait(bar(B_P + (t & 1)), (t >> 1) & 1, wc, 4)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_P + (t & 1)), (t >> 1) & 1, wc, 4))) break;
         tc_fence_after();
         {
           const uint32_t tS = s_buf(t);
           const uint64_t dO_mn = sw128_desc(do_tile(t), L::QHALF, 1024);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks)
-            umma_ts(tdV, tS + a_col(ks), dO_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
+            umma_ts_warp(tdV, tS + a_col(ks), dO_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
         }
         // S^T two tiles ahead, into the buffer P^T(t) occupied (G3 above reads it first)
         if (t + 2 < T) {
-          if (!mbar_wait(bar(B_QFULL + (t + 2) % STAGES), ((t + 2) / STAGES) & 1, wc, 3)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + (t + 2) % STAGES), ((t + 2) / STAGES) & 1, wc, 3))) break;
           tc_fence_after();
           issue_g1(t + 2);
         }
         // dP^T of the next tile as soon as the softmax groups have loaded dP^T(t)
         if (t + 1 < T) {
-          if (!mbar_wait(bar(B_DPFREE), t & 1, wc, 14)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DPFREE), t & 1, wc, 14))) break;
           tc_fence_after();
           issue_g2(t + 1);
         }
         // G4: dK += dS^T Q  (dS^T from its smem tile, K-major; contraction over the query rows)
-        if (!mbar_wait(bar(B_DS), t & 1, wc, 5)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DS), t & 1, wc, 5))) break;
         tc_fence_after();
         {
           const uint64_t dQ_mn = sw128_desc(q_tile(t), L::QHALF, 1024);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks)
-            umma_ss(tdK, dS_k + static_cast<uint64_t>((ks * 32) >> 4), dQ_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
+            umma_ss_warp(tdK, dS_k + static_cast<uint64_t>((ks * 32) >> 4), dQ_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
         }
         if constexpr (!DET) {
           // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
           // (for d = 64 the upper 64 lanes are unused)
-          if (t > 0 && !mbar_wait(bar(B_DQEMPTY), (t - 1) & 1, wc, 6)) break;
+          if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_DQEMPTY), (t - 1) & 1, wc, 6))) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
-            umma_ss(tdQ, dK_mn + mnstep(ks), dS_mn + mnstep(ks), ID_Q, ks > 0);
-          umma_commit(bar(B_DQFULL));
+            umma_ss_warp(tdQ, dK_mn + mnstep(ks), dS_mn + mnstep(ks), ID_Q, ks > 0);
+          umma_commit_warp(bar(B_DQFULL));
         }
-        umma_commit(bar(B_DSFREE));
-        umma_commit(bar(B_QEMPTY + s));
+        umma_commit_warp(bar(B_DSFREE));
+        umma_commit_warp(bar(B_QEMPTY + s));
       }
-      umma_commit(bar(B_ACC));
+      umma_commit_warp(bar(B_ACC));
       if (*abort_flag) drain_wait(bar(B_ACC), 0);
     }
   } else if (warp >= 4 && warp < 12) {
