@@ -97,7 +97,7 @@ Workspace carve(void* ws, int B, int Hq, int Nq, int d, int deterministic) {
   const size_t rows = static_cast<size_t>(B) * Hq * round_up(Nq, kRowPad);
   uint8_t* p = static_cast<uint8_t*>(ws);
   Workspace w;
-  w.Lg = reinterpret_cast<float*>(p);
+  w.nLg = reinterpret_cast<float*>(p);
   w.Dv = reinterpret_cast<float*>(p + align_up(rows * sizeof(float)));
   w.dq_acc = deterministic ? nullptr : reinterpret_cast<float*>(p + 2 * align_up(rows * sizeof(float)));
   (void)d;

@@ -4,8 +4,9 @@
 //   product of flash_attention_backward.cu, rustytorch rtx-flash-attention,
 //   block "Compute row-wise dot product: dO * O"; the D / delta input of the
 //   Triton kernel in triton #1806), computed once per row instead of once per
-//   CTA.  Fused with it: L*log2(e) per row (the main kernel evaluates
-//   exp(S - L) as exp2(S*scale*log2e - L*log2e)), +inf / 0 on the padding rows
+//   CTA.  Fused with it: -L*log2(e) per row (the main kernel evaluates
+//   exp(S - L) as exp2(S*scale*log2e + (-L*log2e)), one fused multiply-add),
+//   -inf / 0 on the padding rows
 //   so that padded query rows contribute exactly zero, and the zeroing of the
 //   fp32 dQ accumulator (triton #1806 allocates it zero-filled).
 // convert: dQ = scale * accumulator, rounded once to the 16-bit dtype.
@@ -38,7 +39,7 @@ __device__ __forceinline__ void widen8(const uint4& u, float (&f)[8]) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
-                  float* __restrict__ Lg, float* __restrict__ Dv, float4* __restrict__ dq_acc,
+                  float* __restrict__ nLg, float* __restrict__ Dv, float4* __restrict__ dq_acc,
                   long long rows, int Nq, int NqPad) {
   constexpr int TPR = D / 8;                 // lanes per row
   constexpr int RPB = 256 / TPR;             // rows per block per sweep
@@ -64,7 +65,7 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     if (!valid) continue;
     if (sub == 0) {
       Dv[row] = acc;
-      Lg[row] = (r < Nq) ? lse[bh * Nq + r] * 1.4426950408889634f : __int_as_float(0x7f800000);
+      nLg[row] = (r < Nq) ? -lse[bh * Nq + r] * 1.4426950408889634f : __int_as_float(0xff800000);
     }
     if (dq_acc != nullptr) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -134,7 +135,7 @@ cudaError_t pre_t(const Problem& pb, const void* o, const void* dO, const float*
   const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.NqPad;
   const long long grid = grid_for(rows, 256 / (D / 8));
   preprocess_kernel<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws.Lg, ws.Dv,
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws.nLg, ws.Dv,
       pb.deterministic ? nullptr : reinterpret_cast<float4*>(ws.dq_acc), rows, pb.Nq, pb.NqPad);
   return cudaGetLastError();
 }

@@ -50,7 +50,7 @@ struct Layout {
 enum : int { B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_DP, B_DS, B_ACC, B_END };
 
 struct Params {
-  const float* Lg;
+  const float* nLg;
   const float* Dv;
   void* dq;
   unsigned int* status;
@@ -126,7 +126,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tma_load_3d(sb + L::OFF_DO + hh * L::HALF, &tm_do, bar(B_Q), 64 * hh, q0, bh);
       }
       const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
-      bulk_load(sb + L::OFF_LD, p.Lg + row, BQ * 4, bar(B_Q));
+      bulk_load(sb + L::OFF_LD, p.nLg + row, BQ * 4, bar(B_Q));
       bulk_load(sb + L::OFF_LD + BQ * 4, p.Dv + row, BQ * 4, bar(B_Q));
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -195,7 +195,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int q = q0 + r;
     bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 25));
     const float* LD = reinterpret_cast<const float*>(smem + L::OFF_LD);
-    const float lq = ok ? LD[r] : 0.f;
+    const float nlq = ok ? LD[r] : 0.f;                // -L*log2(e) of this query row
     const float dq_ = ok ? LD[BQ + r] : 0.f;
     for (int t = 0; ok && t < T; ++t) {
       const int kv0 = t * BK;
@@ -214,8 +214,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
           const int c = ch * 32 + 2 * c2;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c2]), p.scale_log2, -lq));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c2 + 1]), p.scale_log2, -lq));
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c2]), p.scale_log2, nlq));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c2 + 1]), p.scale_log2, nlq));
           if (c >= lim) p0 = 0.f;
           if (c + 1 >= lim) p1 = 0.f;
           pk[c2] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * c2]) - dq_),
@@ -274,7 +274,7 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   Params p;
-  p.Lg = a.ws.Lg;
+  p.nLg = a.ws.nLg;
   p.Dv = a.ws.Dv;
   p.dq = a.dq;
   p.status = a.status;

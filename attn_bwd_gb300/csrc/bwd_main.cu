@@ -72,7 +72,7 @@ struct Layout {
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_BYTES;
   static constexpr int DS_BYTES = BN * BM * 2;    // dS^T, 128 rows x 128 B
   static constexpr int OFF_LD = OFF_DS + DS_BYTES;
-  static constexpr int LD_BYTES = 2 * BM * 4;     // L*log2e and D of one tile
+  static constexpr int LD_BYTES = 2 * BM * 4;     // -L*log2e and D of one tile
   static constexpr int OFF_BAR = OFF_LD + STAGES * LD_BYTES;
   static constexpr int NBAR = 20;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -89,6 +89,7 @@ struct Layout {
   static_assert(COL_DQ + BM <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
+static_assert((STAGES & (STAGES - 1)) == 0, "ring depth must be a power of two");
 
 // barrier indices
 // (S and P have one barrier per S^T buffer: tile t uses buffer t & 1)
@@ -99,7 +100,7 @@ enum : int {
 static_assert(B_END <= 20, "barrier count");
 
 struct Params {
-  const float* Lg;
+  const float* nLg;
   const float* Dv;
   float* dq_acc;
   void* dk;
@@ -212,7 +213,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tma_load_3d(sb + L::OFF_DO + s * L::Q_BYTES + hh * L::QHALF, &tm_do, fb, 64 * hh, q0, bh);
         }
         const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
-        bulk_load(sb + L::OFF_LD + s * L::LD_BYTES, p.Lg + row, BM * 4, fb);
+        bulk_load(sb + L::OFF_LD + s * L::LD_BYTES, p.nLg + row, BM * 4, fb);
         bulk_load(sb + L::OFF_LD + s * L::LD_BYTES + BM * 4, p.Dv + row, BM * 4, fb);
         issued = t + 1;
       }
@@ -336,14 +337,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int kv = kv0 + r;
     const bool row_ok = kv < p.Nkv;
     uint8_t* ds_row = smem + L::OFF_DS + r * 128;
-    for (int t = 0; t < T; ++t) {
-      const int s = t % STAGES;
-      const int q0 = (i0 + t % per_head) * BM;
+    const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
+    int qi = i0;                                          // query tile of tile t (walked, no division)
+    for (int t = 0; t < T; ++t, qi = (qi + 1 == nQt) ? i0 : qi + 1) {
+      const int s = t & (STAGES - 1);
+      const int q0 = qi * BM;
       const float* Ls = reinterpret_cast<const float*>(smem + L::OFF_LD + s * L::LD_BYTES) + 32 * grp;
       const float* Ds = Ls + BM;
       const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BM + 32 * grp;
-      // columns c < lim are masked: key kv lies after query q0 + 32 grp + c
+      // columns c < lim are masked: key kv lies after query q0 + 32 grp + c.
+      // Only KV-tail rows and the diagonal tiles need the per-element test;
+      // the decision is made once per warp.
       const int lim = p.causal ? (kv - q0 - 32 * grp) : INT_MIN;
+      const bool need_mask = __any_sync(0xffffffffu, !row_ok || lim > 0);
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 7))) break;
       tc_fence_after();
       uint32_t pk[16];
@@ -353,16 +359,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_wait();
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(Ls + 4 * c4);
+          // x = S * scale * log2(e) + (-L * log2(e)), two columns per instruction
+          const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(Ls + 4 * c4);
           const int c = 4 * c4;
-          float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 0]), p.scale_log2, -l4.x));
-          float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 1]), p.scale_log2, -l4.y));
-          float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 2]), p.scale_log2, -l4.z));
-          float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 3]), p.scale_log2, -l4.w));
-          if (!row_ok || c + 0 < lim) e0 = 0.f;
-          if (!row_ok || c + 1 < lim) e1 = 0.f;
-          if (!row_ok || c + 2 < lim) e2 = 0.f;
-          if (!row_ok || c + 3 < lim) e3 = 0.f;
+          const float2 xa = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 0]), __uint_as_float(sr[4 * c4 + 1])), sc2, nl.x));
+          const float2 xb = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])), sc2, nl.y));
+          float e0 = ex2_approx(xa.x);
+          float e1 = ex2_approx(xa.y);
+          float e2 = ex2_approx(xb.x);
+          float e3 = ex2_approx(xb.y);
+          if (need_mask) {
+            if (!row_ok || c + 0 < lim) e0 = 0.f;
+            if (!row_ok || c + 1 < lim) e1 = 0.f;
+            if (!row_ok || c + 2 < lim) e2 = 0.f;
+            if (!row_ok || c + 3 < lim) e3 = 0.f;
+          }
           pk[2 * c4] = pack2<BF16>(e0, e1);
           pk[2 * c4 + 1] = pack2<BF16>(e2, e3);
         }
@@ -382,15 +393,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive(bar(B_DPFREE));         // dP^T buffer may now take the next tile's G2
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(Ds + 4 * c4);
+          // dS = P * (dP - D), two columns per instruction
+          const ulonglong2 d2 = *reinterpret_cast<const ulonglong2*>(Ds + 4 * c4);
           const float2 pa = unpack2<BF16>(pk[2 * c4]);
           const float2 pb = unpack2<BF16>(pk[2 * c4 + 1]);
-          const float s0 = pa.x * (__uint_as_float(dr[4 * c4 + 0]) - d4.x);
-          const float s1 = pa.y * (__uint_as_float(dr[4 * c4 + 1]) - d4.y);
-          const float s2 = pb.x * (__uint_as_float(dr[4 * c4 + 2]) - d4.z);
-          const float s3 = pb.y * (__uint_as_float(dr[4 * c4 + 3]) - d4.w);
-          dk[2 * c4] = pack2<BF16>(s0, s1);
-          dk[2 * c4 + 1] = pack2<BF16>(s2, s3);
+          const float2 sa = f2_split(mul_f32x2(f2_bits(pa.x, pa.y),
+              sub_f32x2(f2_bits(__uint_as_float(dr[4 * c4 + 0]), __uint_as_float(dr[4 * c4 + 1])), d2.x)));
+          const float2 sbv = f2_split(mul_f32x2(f2_bits(pb.x, pb.y),
+              sub_f32x2(f2_bits(__uint_as_float(dr[4 * c4 + 2]), __uint_as_float(dr[4 * c4 + 3])), d2.y)));
+          dk[2 * c4] = pack2<BF16>(sa.x, sa.y);
+          dk[2 * c4 + 1] = pack2<BF16>(sbv.x, sbv.y);
         }
       }
       {
@@ -415,9 +427,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int r = threadIdx.x - 384;                     // TMEM lane == column of dQ
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tdQ = tmem + lane_off + L::COL_DQ;
+      int h = hkv * G, qi = i0;                          // head and query tile of tile t
       for (int t = 0; t < T; ++t) {
-        const int h = hkv * G + t / per_head;
-        const int q0 = (i0 + t % per_head) * BM;
+        const int q0 = qi * BM;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), t & 1, wc, 10))) break;
         tc_fence_after();
         uint32_t v0[32], v1[32];
@@ -434,6 +446,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int c = 0; c < 32; ++c) red_add_f32(dst + c * D, __uint_as_float(v0[c]));
 #pragma unroll
           for (int c = 0; c < 32; ++c) red_add_f32(dst + (32 + c) * D, __uint_as_float(v1[c]));
+        }
+        if (++qi == nQt) {
+          qi = i0;
+          ++h;
         }
       }
     }
@@ -489,7 +505,7 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   Params p;
-  p.Lg = a.ws.Lg;
+  p.nLg = a.ws.nLg;
   p.Dv = a.ws.Dv;
   p.dq_acc = a.ws.dq_acc;
   p.dk = a.dk;

@@ -16,7 +16,7 @@ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Workspace carve-up shared by every stage of the backward.
 struct Workspace {
-  float* Lg;      // [B*Hq*NqPad]   L * log2(e); +inf on padding rows
+  float* nLg;     // [B*Hq*NqPad]   -L * log2(e); -inf on padding rows
   float* Dv;      // [B*Hq*NqPad]   rowsum(dO o O); 0 on padding rows
   float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
 };

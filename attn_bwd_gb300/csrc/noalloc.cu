@@ -61,7 +61,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   void* ws = nullptr;
   const int st = static_scratch(&ws);
   if (st != FA_OK) return st;
-  // Every stage rewrites what it later reads (L*log2e, D, and the zeroed dQ
+  // Every stage rewrites what it later reads (-L*log2e, D, and the zeroed dQ
   // accumulator), so whatever an earlier call left in the array is irrelevant.
   return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic, ws,
                 FA_STATIC_SCRATCH_BYTES, stream);

@@ -78,7 +78,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 
 /*
  * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs.
- * Holds D = rowsum(dO o O) and L*log2(e) per query row (rows padded to a
+ * Holds D = rowsum(dO o O) and -L*log2(e) per query row (rows padded to a
  * multiple of 128), plus, when deterministic == 0, the fp32 dQ accumulator
  * [B, Hq, Nq padded, d] of the sequence-parallel scheme (triton #1806,
  * "Minimal Repro": dq is an fp32 buffer that every KV-tile program adds to).
@@ -106,7 +106,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  * fa_bwd_preprocess -- step 1 of fa_bwd: D_i = sum_c dO_ic O_ic (fp32), the
  * row-wise dot product the pages precompute (flash_attention_backward.cu,
  * "Compute row-wise dot product: dO * O"; the D input of the Triton kernel in
- * triton #1806), L*log2(e) per row, and (deterministic == 0) zeroes the fp32
+ * triton #1806), -L*log2(e) per row, and (deterministic == 0) zeroes the fp32
  * dQ accumulator.  Writes only the workspace.
  */
 int fa_bwd_preprocess(const void* o, const void* dO, const float* lse,

@@ -151,7 +151,7 @@ def test_extra_shapes(shape, det):
 # ------------------------------------------------------------ step-level checks
 
 def test_preprocess_rowdot_and_padding():
-    """Step 1 alone: D = rowsum(dO o O) from the given O, L*log2(e), and padding rows."""
+    """Step 1 alone: D = rowsum(dO o O) from the given O, -L*log2(e), and padding rows."""
     shape = inputs.Shape(2, 3, 3, 100, 100, 128, False, "bf16")
     q, k, v, do = (t.cuda() for t in inputs.draw(shape, 7))
     o, lse = torch_api.forward(q, k, v, shape.softmax_scale, False)
@@ -163,14 +163,14 @@ def test_preprocess_rowdot_and_padding():
     torch.cuda.synchronize()
     rows = 2 * 3 * 128
     f = ws.view(torch.float32)
-    Lg = f[:rows].view(2, 3, 128).cpu().double().numpy()
+    nLg = f[:rows].view(2, 3, 128).cpu().double().numpy()
     Dv = f[rows:2 * rows].view(2, 3, 128).cpu().double().numpy()
     acc = f[2 * rows:2 * rows + rows * 128]
     D_ref = (_np(o) * _np(do)).sum(-1)
     np.testing.assert_allclose(Dv[:, :, :100], D_ref, rtol=1e-5, atol=1e-5)
     assert (Dv[:, :, 100:] == 0).all()
-    np.testing.assert_allclose(Lg[:, :, :100], _np(lse) * np.log2(np.e), rtol=1e-6, atol=1e-6)
-    assert np.isinf(Lg[:, :, 100:]).all() and (Lg[:, :, 100:] > 0).all()
+    np.testing.assert_allclose(nLg[:, :, :100], -_np(lse) * np.log2(np.e), rtol=1e-6, atol=1e-6)
+    assert np.isinf(nLg[:, :, 100:]).all() and (nLg[:, :, 100:] < 0).all()
     assert (acc == 0).all()
 
 
