@@ -74,7 +74,7 @@ struct Layout {
   static constexpr int OFF_LD = OFF_DS + DS_BYTES;
   static constexpr int LD_BYTES = 2 * BM * 4;     // -L*log2e and D of one tile
   static constexpr int OFF_BAR = OFF_LD + STAGES * LD_BYTES;
-  static constexpr int NBAR = 20;
+  static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = TOTAL + 1024;      // slack for 1024-byte alignment
@@ -94,10 +94,10 @@ static_assert((STAGES & (STAGES - 1)) == 0, "ring depth must be a power of two")
 // barrier indices
 // (S and P have one barrier per S^T buffer: tile t uses buffer t & 1)
 enum : int {
-  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_DP = B_P + 2, B_DPFREE, B_DS,
-  B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_END
+  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_SFREE = B_P + 2,
+  B_DP = B_SFREE + 2, B_DPFREE, B_DS, B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_AFIN, B_END
 };
-static_assert(B_END <= 20, "barrier count");
+static_assert(B_END <= 24, "barrier count");
 
 struct Params {
   const float* nLg;
@@ -166,7 +166,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_S + i), 1);
       mbar_init(bar(B_P + i), 256);
+      mbar_init(bar(B_SFREE + i), 1);
     }
+    mbar_init(bar(B_AFIN), 1);
     mbar_init(bar(B_DP), 1);
     mbar_init(bar(B_DPFREE), 256);
     mbar_init(bar(B_DS), 256);
@@ -222,9 +224,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int t = max(0, issued - STAGES); t < issued; ++t)
         drain_wait(bar(B_QFULL + t % STAGES), (t / STAGES) & 1);
     }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    if (T > 0) {   // the whole warp walks the loop; elect.sync issues each MMA
+  } else if (warp == 1 || warp == 2) {
+    // ================================================================ MMA issuers
+    // Two warps issue tcgen05.mma, each walking its loop with all 32 lanes
+    // (elect.sync picks the issuing lane):
+    //   warp 1: G1 (S^T) and G2 (dP^T), the products the softmax groups consume;
+    //   warp 2: G3, G4, G5, the products of what the softmax groups produce.
+    // Each blocks only on its own inputs, so dK/dQ of tile t are issued as soon
+    // as dS^T(t) exists instead of queueing behind later tiles' S^T and dP^T.
+    // Every hand-off between the two streams is an mbarrier: G1 into an S^T
+    // buffer waits for the G3 that read the P^T there (s_free).
+    if (T > 0) {
       constexpr uint32_t ID_S = make_idesc_f16(128, BM, BF16, false, false);
       constexpr uint32_t ID_KV = make_idesc_f16(128, D, BF16, false, true);   // A K-major (TMEM or smem), B MN-major
       constexpr uint32_t ID_Q = make_idesc_f16(128, BM, BF16, true, true);
@@ -232,10 +242,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t tdK = tmem + L::COL_DK, tdV = tmem + L::COL_DV, tdQ = tmem + L::COL_DQ;
       const uint32_t aK = sb + L::OFF_K, aV = sb + L::OFF_V;
       auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BM; };
-      auto q_tile = [&](int t) -> uint32_t { return sb + L::OFF_Q + (t % STAGES) * L::Q_BYTES; };
-      auto do_tile = [&](int t) -> uint32_t { return sb + L::OFF_DO + (t % STAGES) * L::Q_BYTES; };
-      // One thread issues every MMA, so per-instruction work is kept minimal:
-      // each operand tile's descriptor is built once and stepped by
+      auto q_tile = [&](int t) -> uint32_t { return sb + L::OFF_Q + (t & (STAGES - 1)) * L::Q_BYTES; };
+      auto do_tile = [&](int t) -> uint32_t { return sb + L::OFF_DO + (t & (STAGES - 1)) * L::Q_BYTES; };
+      // Each operand tile's descriptor is built once and stepped by
       // compile-time offsets (the start address is the descriptor's low field,
       // so adding offset >> 4 advances it).
       const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aV, 16, 1024);
@@ -248,85 +257,81 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       };
       // MN-major step ks: 16 rows of 128 bytes
       auto mnstep = [](int ks) -> uint64_t { return static_cast<uint64_t>((ks * 2048) >> 4); };
-      // G1: S^T = K Q^T  (contraction over d, 16 per instruction)
-      auto issue_g1 = [&](int t) {
-        const uint64_t dQ_k = sw128_desc(q_tile(t), 16, 1024);
-        const uint32_t tS = s_buf(t);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_ss_warp(tS, dK_k + kstep(ks, L::KHALF), dQ_k + kstep(ks, L::QHALF), ID_S, ks > 0);
-        umma_commit_warp(bar(B_S + (t & 1)));
-      };
-      // G2: dP^T = V dO^T
-      auto issue_g2 = [&](int t) {
-        const uint64_t dO_k = sw128_desc(do_tile(t), 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_ss_warp(tdP, dV_k + kstep(ks, L::KHALF), dO_k + kstep(ks, L::QHALF), ID_S, ks > 0);
-        umma_commit_warp(bar(B_DP));
-      };
       // 16-bit A operand column for query rows [16ks, 16ks+16): group ks/2, second half if ks odd
       auto a_col = [](int ks) -> uint32_t { return static_cast<uint32_t>(32 * (ks >> 1) + 8 * (ks & 1)); };
+      auto wait = [&](uint32_t b, uint32_t parity, uint32_t site) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+      };
 
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KV), 0, wc, 2)) && __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL), 0, wc, 3));
-      if (ok) {
-        tc_fence_after();
-        issue_g1(0);
-        issue_g2(0);
-        if (T > 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + 1), 0, wc, 3));
+      if (warp == 1) {
+        bool ok = wait(bar(B_KV), 0, 2);
+        for (int t = 0; ok && t < T; ++t) {
+          // G1: S^T(t) = K Q^T  (contraction over d, 16 per instruction), into buffer t & 1
+          if (!wait(bar(B_QFULL + (t & (STAGES - 1))), (t / STAGES) & 1, 3)) break;
+          if (t >= 2 && !wait(bar(B_SFREE + (t & 1)), ((t - 2) >> 1) & 1, 15)) break;
           tc_fence_after();
-          if (ok) issue_g1(1);
+          {
+            const uint64_t dQ_k = sw128_desc(q_tile(t), 16, 1024);
+            const uint32_t tS = s_buf(t);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_warp(tS, dK_k + kstep(ks, L::KHALF), dQ_k + kstep(ks, L::QHALF), ID_S, ks > 0);
+            umma_commit_warp(bar(B_S + (t & 1)));
+          }
+          // G2: dP^T(t) = V dO^T, once the softmax groups have loaded dP^T(t-1)
+          if (t >= 1 && !wait(bar(B_DPFREE), (t - 1) & 1, 14)) break;
+          tc_fence_after();
+          {
+            const uint64_t dO_k = sw128_desc(do_tile(t), 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_warp(tdP, dV_k + kstep(ks, L::KHALF), dO_k + kstep(ks, L::QHALF), ID_S, ks > 0);
+            umma_commit_warp(bar(B_DP));
+          }
         }
+        // this warp's MMAs must have completed before TMEM is released
+        umma_commit_warp(bar(B_AFIN));
+        drain_wait(bar(B_AFIN), 0);
+      } else {
+        for (int t = 0; t < T; ++t) {
+          // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
+          if (!wait(bar(B_P + (t & 1)), (t >> 1) & 1, 4)) break;
+          tc_fence_after();
+          {
+            const uint32_t tS = s_buf(t);
+            const uint64_t dO_mn = sw128_desc(do_tile(t), L::QHALF, 1024);
+#pragma unroll
+            for (int ks = 0; ks < BM / 16; ++ks)
+              umma_ts_warp(tdV, tS + a_col(ks), dO_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
+            umma_commit_warp(bar(B_SFREE + (t & 1)));
+          }
+          // G4: dK += dS^T Q  (dS^T from its smem tile, K-major; contraction over the query rows)
+          if (!wait(bar(B_DS), t & 1, 5)) break;
+          tc_fence_after();
+          {
+            const uint64_t dQ_mn = sw128_desc(q_tile(t), L::QHALF, 1024);
+#pragma unroll
+            for (int ks = 0; ks < BM / 16; ++ks)
+              umma_ss_warp(tdK, dS_k + static_cast<uint64_t>((ks * 32) >> 4), dQ_mn + mnstep(ks), ID_KV,
+                           (t > 0 || ks > 0));
+          }
+          if constexpr (!DET) {
+            // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
+            // (for d = 64 the upper 64 lanes are unused)
+            if (t > 0 && !wait(bar(B_DQEMPTY), (t - 1) & 1, 6)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+              umma_ss_warp(tdQ, dK_mn + mnstep(ks), dS_mn + mnstep(ks), ID_Q, ks > 0);
+            umma_commit_warp(bar(B_DQFULL));
+          }
+          umma_commit_warp(bar(B_DSFREE));
+          // stage of tile t: G1/G2(t) have completed (P(t), dS(t) depend on them), G3/G4(t) are tracked here
+          umma_commit_warp(bar(B_QEMPTY + (t & (STAGES - 1))));
+        }
+        umma_commit_warp(bar(B_ACC));
+        if (*abort_flag) drain_wait(bar(B_ACC), 0);
       }
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % STAGES;
-        // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_P + (t & 1)), (t >> 1) & 1, wc, 4))) break;
-        tc_fence_after();
-        {
-          const uint32_t tS = s_buf(t);
-          const uint64_t dO_mn = sw128_desc(do_tile(t), L::QHALF, 1024);
-#pragma unroll
-          for (int ks = 0; ks < BM / 16; ++ks)
-            umma_ts_warp(tdV, tS + a_col(ks), dO_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
-        }
-        // S^T two tiles ahead, into the buffer P^T(t) occupied (G3 above reads it first)
-        if (t + 2 < T) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + (t + 2) % STAGES), ((t + 2) / STAGES) & 1, wc, 3))) break;
-          tc_fence_after();
-          issue_g1(t + 2);
-        }
-        // dP^T of the next tile as soon as the softmax groups have loaded dP^T(t)
-        if (t + 1 < T) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DPFREE), t & 1, wc, 14))) break;
-          tc_fence_after();
-          issue_g2(t + 1);
-        }
-        // G4: dK += dS^T Q  (dS^T from its smem tile, K-major; contraction over the query rows)
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DS), t & 1, wc, 5))) break;
-        tc_fence_after();
-        {
-          const uint64_t dQ_mn = sw128_desc(q_tile(t), L::QHALF, 1024);
-#pragma unroll
-          for (int ks = 0; ks < BM / 16; ++ks)
-            umma_ss_warp(tdK, dS_k + static_cast<uint64_t>((ks * 32) >> 4), dQ_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
-        }
-        if constexpr (!DET) {
-          // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
-          // (for d = 64 the upper 64 lanes are unused)
-          if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_DQEMPTY), (t - 1) & 1, wc, 6))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks)
-            umma_ss_warp(tdQ, dK_mn + mnstep(ks), dS_mn + mnstep(ks), ID_Q, ks > 0);
-          umma_commit_warp(bar(B_DQFULL));
-        }
-        umma_commit_warp(bar(B_DSFREE));
-        umma_commit_warp(bar(B_QEMPTY + s));
-      }
-      umma_commit_warp(bar(B_ACC));
-      if (*abort_flag) drain_wait(bar(B_ACC), 0);
     }
   } else if (warp >= 4 && warp < 12) {
     // ================================================================ softmax / dS groups
