@@ -56,6 +56,22 @@ def flops(sh) -> float:
     return f / 2 if sh.causal else f
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's figure: the whole job is done only when every replica is."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Every replica runs the same workload (weak scaling): total FLOPs of all ranks / slowest time."""
+    return world * flops_per_step * steps / (ms_max * 1e-3) / 1e12
+
+
 def config_dict(sh, det, n_gpus):
     in_bytes = 2 * (2 * sh.B * sh.Hq * sh.Nq * sh.d + 3 * sh.B * sh.Hkv * sh.Nkv * sh.d) + 4 * sh.B * sh.Hq * sh.Nq
     return {"workload": f"llama3-8b-shaped GQA causal attention backward B={sh.B} Hq={sh.Hq} Hkv={sh.Hkv} "
@@ -252,15 +268,12 @@ def main():
             dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     main_ms = [a.elapsed_time(b) for a, b in evs]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     if _lib.fa_last_device_error(stream) != 0:
         raise RuntimeError("device status reported a failure in the timed region")
 
     fl = flops(sh)
-    value = world * fl * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(fl, args.steps, world, ms_total)
     peaks, peaks_src = load_peaks()
     main_avg = sum(main_ms) / len(main_ms)
     achieved = fl / (main_avg * 1e-3) / 1e12
@@ -297,11 +310,8 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * fl * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_val = whole_job_tflops(fl, e2e_steps, world, e2e_ms)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
