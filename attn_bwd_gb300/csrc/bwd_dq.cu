@@ -10,8 +10,19 @@
 //   G2  dP [BQ x BK] = dO . V^T      A = dO (smem, K-major), B = V (K-major)
 //   G5  dQ [BQ x d ] += dS . K       A = dS (TMEM, 16-bit),  B = K (MN-major)
 // and dQ = scale * dQ is written once in the 16-bit dtype.
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
-// issuer, warps 4-7 thread r owns query row r (TMEM lane r).
+//
+// Warp roles (384 threads):
+//   warp 0       TMA producer: Q, dO, -L*log2e, D once; K, V through a 2-stage ring
+//   warp 1       owns TMEM; issues G1 and G2 (the products the softmax groups consume)
+//   warp 2       issues G5 (the product of what the softmax groups produce)
+//   warps 4-11   two softmax groups: thread r of group g owns query row r (TMEM
+//                lane r) and KV columns [64g, 64g+64) of each tile
+// S is double-buffered in TMEM (S0, S1, dP, dQ = 4 x 128 columns); the dP
+// buffer is released as soon as the softmax groups have loaded it, so G2 of
+// the next tile overlaps their arithmetic; dS (16-bit) is packed into the S
+// buffer it came from and read from there by G5.  The two issuing warps walk
+// their loops with all lanes and elect.sync issues each MMA; every hand-off is
+// an mbarrier with one arrival per warp.
 #include <cstdint>
 #include <climits>
 
@@ -24,7 +35,7 @@ namespace {
 constexpr int BQ = 128;    // query rows per CTA (TMEM lanes)
 constexpr int BK = 128;    // KV rows per step
 constexpr int STAGES = 2;  // K/V ring depth
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 
 template <int D>
 struct Layout {
@@ -36,18 +47,22 @@ struct Layout {
   static constexpr int OFF_KV = 2 * TILE;       // stage s: K at OFF_KV + 2*s*TILE, V after it
   static constexpr int OFF_LD = OFF_KV + STAGES * 2 * TILE;
   static constexpr int OFF_BAR = OFF_LD + 2 * BQ * 4;
-  static constexpr int NBAR = 12;
+  static constexpr int NBAR = 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = (TOTAL + 1024) > 120 * 1024 ? (TOTAL + 1024) : 120 * 1024;
-  static constexpr int COL_S = 0;
-  static constexpr int COL_DP = BK;
-  static constexpr int COL_DQ = 2 * BK;
+  static constexpr int COL_S = 0;               // buffers at 0 and BK
+  static constexpr int COL_DP = 2 * BK;
+  static constexpr int COL_DQ = 3 * BK;
   static_assert(COL_DQ + D <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-enum : int { B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_DP, B_DS, B_ACC, B_END };
+enum : int {
+  B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_DS = B_S + 2, B_SFREE = B_DS + 2,
+  B_DP = B_SFREE + 2, B_DPFREE, B_ACC, B_AFIN, B_END
+};
+static_assert(B_END <= 16, "barrier count");
 
 struct Params {
   const float* nLg;
@@ -100,10 +115,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(bar(B_KVFULL + s), 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
     }
-    mbar_init(bar(B_S), 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(bar(B_S + j), 1);
+      mbar_init(bar(B_DS + j), 8);      // one arrival per softmax warp
+      mbar_init(bar(B_SFREE + j), 1);
+    }
     mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_DS), 128);
+    mbar_init(bar(B_DPFREE), 8);
     mbar_init(bar(B_ACC), 1);
+    mbar_init(bar(B_AFIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -118,6 +138,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const WaitCtx wc{p.status, abort_flag};
 
   if (warp == 0) {
+    // ================================================================ TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(B_Q), 2 * L::TILE + 2 * BQ * 4);
 #pragma unroll
@@ -147,101 +168,136 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int t = max(0, issued - STAGES); t < issued; ++t)
         drain_wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1);
     }
-  } else if (warp == 1) {
-    {   // the whole warp walks the loop; elect.sync issues each MMA
+  } else if (warp == 1 || warp == 2) {
+    // ================================================================ MMA issuers
+    if (T > 0) {
       constexpr uint32_t ID_S = make_idesc_f16(128, BK, BF16, false, false);
       constexpr uint32_t ID_Q = make_idesc_f16(128, D, BF16, false, true);
-      const uint32_t tS = tmem + L::COL_S, tdP = tmem + L::COL_DP, tdQ = tmem + L::COL_DQ;
+      const uint32_t tdP = tmem + L::COL_DP, tdQ = tmem + L::COL_DQ;
       const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q, 16, 1024), dO_k = sw128_desc(sb + L::OFF_DO, 16, 1024);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 22));
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % STAGES;
-        const uint32_t ph = (t / STAGES) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_KVFULL + s), ph, wc, 23))) break;
-        tc_fence_after();
-        const uint32_t aK = sb + L::OFF_KV + s * 2 * L::TILE;
-        const uint32_t aV = aK + L::TILE;
-        // descriptors built once per tile, stepped by compile-time offsets >> 4
-        const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aV, 16, 1024);
-        const uint64_t dK_mn = sw128_desc(aK, L::HALF, 1024);
+      auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BK; };
+      auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_KV + (t % STAGES) * 2 * L::TILE; };
+      // K-major step ks (16 elements of d): 64-column half ks/4, 32 bytes per step inside it
+      auto kstep = [](int ks) -> uint64_t {
+        return static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
+      };
+      auto wait = [&](uint32_t bb, uint32_t parity, uint32_t site) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bb, parity, wc, site));
+      };
+      if (warp == 1) {
+        bool ok = wait(bar(B_Q), 0, 22);
+        for (int t = 0; ok && t < T; ++t) {
+          if (!wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1, 23)) break;
+          if (t >= 2 && !wait(bar(B_SFREE + (t & 1)), ((t - 2) >> 1) & 1, 24)) break;
+          tc_fence_after();
+          const uint32_t aK = k_tile(t);
+          const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aK + L::TILE, 16, 1024);
+          // G1: S = Q K^T into buffer t & 1
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t o = static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
-          umma_ss_warp(tS, dQ_k + o, dK_k + o, ID_S, ks > 0);
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss_warp(s_buf(t), dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
+          umma_commit_warp(bar(B_S + (t & 1)));
+          // G2: dP = dO V^T, once the softmax groups have loaded dP of the previous tile
+          if (t >= 1 && !wait(bar(B_DPFREE), (t - 1) & 1, 25)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss_warp(tdP, dO_k + kstep(ks), dV_k + kstep(ks), ID_S, ks > 0);
+          umma_commit_warp(bar(B_DP));
         }
-        umma_commit_warp(bar(B_S));
+        umma_commit_warp(bar(B_AFIN));   // this warp's MMAs complete before TMEM is released
+        drain_wait(bar(B_AFIN), 0);
+      } else {
+        for (int t = 0; t < T; ++t) {
+          // G5: dQ += dS K  (dS, 16-bit, packed into the first half of each group's
+          // 64 columns of the S buffer; K read MN-major)
+          if (!wait(bar(B_DS + (t & 1)), (t >> 1) & 1, 26)) break;
+          tc_fence_after();
+          const uint64_t dK_mn = sw128_desc(k_tile(t), L::HALF, 1024);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t o = static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
-          umma_ss_warp(tdP, dO_k + o, dV_k + o, ID_S, ks > 0);
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_ts_warp(tdQ, s_buf(t) + 64 * (ks >> 2) + 8 * (ks & 3),
+                         dK_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_Q, (t > 0 || ks > 0));
+          umma_commit_warp(bar(B_SFREE + (t & 1)));
+          // stage of tile t: G1/G2(t) have completed (dS(t) depends on them); G5(t) is tracked here
+          umma_commit_warp(bar(B_KVEMPTY + t % STAGES));
         }
-        umma_commit_warp(bar(B_DP));
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DS), t & 1, wc, 24))) break;
-        tc_fence_after();
-        // dQ += dS K: dS (16-bit) in the first BK/2 columns of S, K read MN-major
-#pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks)
-          umma_ts_warp(tdQ, tS + ks * 8, dK_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_Q, (t > 0 || ks > 0));
-        umma_commit_warp(bar(B_KVEMPTY + s));
+        umma_commit_warp(bar(B_ACC));
+        if (*abort_flag) drain_wait(bar(B_ACC), 0);
       }
-      umma_commit_warp(bar(B_ACC));
-      if (*abort_flag) drain_wait(bar(B_ACC), 0);
     }
   } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;                  // query row == TMEM lane
+    // ================================================================ softmax / dS groups
+    const int grp = (warp - 4) >> 2;                    // KV columns [64 grp, 64 grp + 64)
+    const int r = threadIdx.x - 128 - 128 * grp;       // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + L::COL_S;
-    const uint32_t tdP = tmem + lane_off + L::COL_DP;
+    const uint32_t tdP = tmem + lane_off + L::COL_DP + 64 * grp;
     const int q = q0 + r;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 25));
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 27));
     const float* LD = reinterpret_cast<const float*>(smem + L::OFF_LD);
     const float nlq = ok ? LD[r] : 0.f;                // -L*log2(e) of this query row
     const float dq_ = ok ? LD[BQ + r] : 0.f;
+    const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
+    const uint64_t nl2 = f2_bits(nlq, nlq);
+    const uint64_t dd2 = f2_bits(dq_, dq_);
     for (int t = 0; ok && t < T; ++t) {
       const int kv0 = t * BK;
       // columns c >= lim are masked: past the end of K/V, or (causal) after query q
-      int lim = p.Nkv - kv0;
-      if (p.causal) lim = min(lim, q - kv0 + 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S), t & 1, wc, 26))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 27))) break;
+      int lim = p.Nkv - kv0 - 64 * grp;
+      if (p.causal) lim = min(lim, q - kv0 - 64 * grp + 1);
+      const bool need_mask = __any_sync(0xffffffffu, lim < 64);
+      const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK + 64 * grp;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 28))) break;
+      tc_fence_after();
+      uint32_t dr[64];
+      tmem_ld_x32(tdP, *reinterpret_cast<uint32_t(*)[32]>(dr));
+      tmem_ld_x32(tdP + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DPFREE));       // the dP buffer may take the next tile's G2
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 29))) break;
       tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < BK / 32; ++ch) {
-        uint32_t sr[32], dr[32], pk[16];
-        tmem_ld_x32(tS + ch * 32, sr);
-        tmem_ld_x32(tdP + ch * 32, dr);
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sr[32], pk[16];
+        tmem_ld_x32(tS + 32 * ch, sr);
         tmem_ld_wait();
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
-          const int c = ch * 32 + 2 * c2;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c2]), p.scale_log2, nlq));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c2 + 1]), p.scale_log2, nlq));
-          if (c >= lim) p0 = 0.f;
-          if (c + 1 >= lim) p1 = 0.f;
-          pk[c2] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * c2]) - dq_),
-                               p1 * (__uint_as_float(dr[2 * c2 + 1]) - dq_));
+          const int c = 32 * ch + 2 * c2;
+          const float2 x = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1])), sc2, nl2));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
+          if (need_mask) {
+            if (c >= lim) p0 = 0.f;
+            if (c + 1 >= lim) p1 = 0.f;
+          }
+          const float2 ds = f2_split(mul_f32x2(f2_bits(p0, p1),
+              sub_f32x2(f2_bits(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), dd2)));
+          pk[c2] = pack2<BF16>(ds.x, ds.y);
         }
-        // columns [16ch, 16ch+16) of S were already read (chunk ch covers [32ch, 32ch+32))
-        tmem_st_x16(tS + ch * 16, pk);
+        // columns [16ch, 16ch+16) of this group's S columns were already read
+        tmem_st_x16(tS + 16 * ch, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_DS));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DS + (t & 1)));
     }
-    // ---- epilogue: dQ = scale * acc, 16-bit
+    // ---- epilogue: dQ = scale * acc, 16-bit; group g writes columns [D/2 g, D/2 (g+1))
     bool have = ok && T > 0;
     if (have) {
-      have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 28));
+      have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 30));
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
     uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + (static_cast<size_t>(bh) * p.Nq + q) * D * 2;
 #pragma unroll 1
-    for (int ch = 0; ch < D / 32; ++ch) {
+    for (int ch = 0; ch < D / 64; ++ch) {
+      const int col = (D / 2) * grp + 32 * ch;
       uint32_t pk[16];
       if (have) {
         uint32_t v[32];
-        tmem_ld_x32(tmem + lane_off + L::COL_DQ + ch * 32, v);
+        tmem_ld_x32(tmem + lane_off + L::COL_DQ + col, v);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 16; ++c)
@@ -251,7 +307,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
       if (q < p.Nq && !aborted) {
-        uint4* d4 = reinterpret_cast<uint4*>(out + ch * 64);
+        uint4* d4 = reinterpret_cast<uint4*>(out + col * 2);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
       }

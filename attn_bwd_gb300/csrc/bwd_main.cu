@@ -165,15 +165,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_S + i), 1);
-      mbar_init(bar(B_P + i), 256);
+      mbar_init(bar(B_P + i), 8);        // one arrival per softmax warp
       mbar_init(bar(B_SFREE + i), 1);
     }
     mbar_init(bar(B_AFIN), 1);
     mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_DPFREE), 256);
-    mbar_init(bar(B_DS), 256);
+    mbar_init(bar(B_DPFREE), 8);
+    mbar_init(bar(B_DS), 8);
     mbar_init(bar(B_DQFULL), 1);
-    mbar_init(bar(B_DQEMPTY), 128);
+    mbar_init(bar(B_DQEMPTY), 4);      // one arrival per dQ warp
     mbar_init(bar(B_DSFREE), 1);
     mbar_init(bar(B_ACC), 1);
     *abort_flag = 0;
@@ -386,7 +386,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_st_x16(tS, pk);                  // P^T, 16-bit, over the columns just read
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_P + (t & 1)));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P + (t & 1)));
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 8))) break;
       tc_fence_after();
       uint32_t dk[16];
@@ -395,7 +396,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_x32(tdP, dr);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(bar(B_DPFREE));         // dP^T buffer may now take the next tile's G2
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DPFREE));   // dP^T buffer may now take the next tile's G2
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           // dS = P * (dP - D), two columns per instruction
@@ -424,7 +426,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         fence_proxy_async_smem();
       }
-      mbar_arrive(bar(B_DS));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DS));
     }
   } else if (warp >= 12) {
     // ================================================================ dQ group
@@ -442,7 +445,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_x32(tdQ + 32, v1);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(bar(B_DQEMPTY));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DQEMPTY));
         // Thread r holds column r of the 64 x d tile: for each query row, the 32
         // lanes of a warp add one contiguous 128-byte segment of the accumulator.
         if (r < D) {
