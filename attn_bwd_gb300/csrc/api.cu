@@ -164,7 +164,15 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   FwdArgs a;
   a.pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, 1);
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  return cuda_status(launch_fwd(a, stream));
+  if ((st = get_encoder())) return st;
+  unsigned int* status = nullptr;
+  if ((st = status_ptr(&status))) return st;
+  CUtensorMap tq, tk, tv;
+  const int bf = a.pb.bf16;
+  if ((st = make_map(&tq, q, bf, d, Nq, static_cast<long long>(B) * Hq, 128))) return st;
+  if ((st = make_map(&tk, k, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
+  if ((st = make_map(&tv, v, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
+  return cuda_status(launch_fwd(a, tq, tk, tv, status, stream));
 }
 
 int fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int Hq, int Hkv, int Nq, int Nkv,

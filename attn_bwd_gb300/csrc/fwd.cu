@@ -1,14 +1,27 @@
-// fwd.cu -- exact attention forward producing O and the log-sum-exp L that
-// the backward consumes (L is the natural-log LSE of the scaled, masked
-// scores, the convention of flash_attention_backward.cu, rustytorch
-// rtx-flash-attention, block "Compute softmax probabilities from scores and
-// LSE").  This is a plain fp32 CUDA-core kernel with the usual running-max
-// ("online") softmax over 64-row KV tiles; it exists to make inputs for the
-// backward and is deliberately independent of the tensor-core machinery the
-// backward uses.
+// fwd.cu -- exact attention forward on tcgen05 tensor cores, producing O and
+// the log-sum-exp L that the backward consumes (L is the natural-log LSE of the
+// scaled, masked scores: the convention of flash_attention_backward.cu,
+// rustytorch rtx-flash-attention, block "Compute softmax probabilities from
+// scores and LSE").
+//
+// One CTA owns a 128-row query tile of one query head and walks the KV tiles
+// it can see (causal: up to the diagonal), keeping O in TMEM:
+//   G1  S [BQ x BK] = Q . K^T     A = Q (smem, K-major), B = K (K-major)
+//   PV  O [BQ x d ] += P . V      A = P (TMEM, 16-bit),  B = V (MN-major)
+// Softmax runs in the log2 domain (x = S * scale * log2 e) with a running
+// reference max m per row.  P = 2^(x - m) is accumulated unnormalised and O is
+// divided by the row sum once at the end, so any reference max that is the
+// same for O and the sum gives the exact result; m is therefore only moved
+// (and O, sum rescaled by 2^(m_old - m_new)) when the row max exceeds it by
+// more than 8, which keeps P <= 256 and makes rescaling rare after the first
+// tiles.
+//
+// Warp roles (256 threads): warp 0 TMA producer (Q once, K/V ring), warp 1 owns
+// TMEM and issues G1, warp 2 issues PV, warps 4-7 thread r owns query row r
+// (TMEM lane r) and all 128 columns of each S tile.  S is double-buffered in
+// TMEM (S0, S1, O = 2 x 128 + d columns).
 #include <cstdint>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
+#include <climits>
 #include <math_constants.h>
 
 #include "kernels.h"
@@ -17,214 +30,323 @@
 namespace fa {
 namespace {
 
-constexpr int TQ = 64;     // query rows per CTA
-constexpr int TK = 64;     // key rows per step
+constexpr int BQ = 128;     // query rows per CTA (TMEM lanes)
+constexpr int BK = 128;     // KV rows per step
+constexpr int STAGES = 2;   // K/V ring depth
 constexpr int kThreads = 256;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 
 template <int D>
-struct Smem {
-  static constexpr int QS = D + 4;   // row strides (floats) chosen to spread banks
-  static constexpr int KS = D + 1;
-  static constexpr int SS = TK + 1;
-  static constexpr int BYTES = 4 * (TQ * QS + TK * KS + TK * D + TQ * SS + 3 * TQ);
+struct Layout {
+  static constexpr int NH = D / 64;
+  static constexpr int HALF = 128 * 128;        // one 64-column half of a 128-row tile
+  static constexpr int TILE = NH * HALF;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = TILE;           // stage s: K at OFF_KV + 2*s*TILE, V after it
+  static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE;
+  static constexpr int NBAR = 16;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int TOTAL = OFF_MISC + 16;
+  static constexpr int ALLOC = (TOTAL + 1024) > 120 * 1024 ? (TOTAL + 1024) : 120 * 1024;
+  static constexpr int COL_S = 0;               // buffers at 0 and BK
+  static constexpr int COL_O = 2 * BK;
+  static_assert(COL_O + D <= 512, "TMEM budget");
+  static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
+enum : int {
+  B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_SFREE = B_P + 2,
+  B_PV = B_SFREE + 2, B_AFIN, B_END
+};
+static_assert(B_END <= 16, "barrier count");
+
 struct Params {
-  const void* q;
-  const void* k;
-  const void* v;
   void* o;
   float* lse;
+  unsigned int* status;
   int B, Hq, Hkv, Nq, Nkv;
-  float scale;
+  float scale_log2;
   int causal;
 };
 
-template <bool BF16>
-__device__ __forceinline__ void load8(const void* base, long long elem, float* dst) {
-  const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = unpack2<BF16>(w[i]);
-    dst[2 * i] = f.x;
-    dst[2 * i + 1] = f.y;
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;
   }
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads)
-fwd_kernel(const Params p) {
-  using S = Smem<D>;
-  extern __shared__ float sm[];
-  float* Qs = sm;
-  float* Ks = Qs + TQ * S::QS;
-  float* Vs = Ks + TK * S::KS;
-  float* Ss = Vs + TK * D;
-  float* row_m = Ss + TQ * S::SS;
-  float* row_l = row_m + TQ;
-  float* row_a = row_l + TQ;
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
-  const int tid = threadIdx.x;
-  const int ty = tid / 16, tx = tid % 16;
-  const int q0 = blockIdx.x * TQ;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int hk = h / (p.Hq / p.Hkv);
-  const long long qbase = (static_cast<long long>(b) * p.Hq + h) * p.Nq;
-  const long long kbase = (static_cast<long long>(b) * p.Hkv + hk) * p.Nkv;
+  // ---- work item: query tile i of head h of batch b; largest i first (longest under causal)
+  const int BH = p.B * p.Hq;
+  const int nQt = (p.Nq + BQ - 1) / BQ;
+  const int i = nQt - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int b = bh / p.Hq;
+  const int h = bh - b * p.Hq;
+  const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int q0 = i * BQ;
+  const int nKt = (p.Nkv + BK - 1) / BK;
+  const int qmax = min(q0 + BQ, p.Nq) - 1;
+  const int T = p.causal ? min(nKt, qmax / BK + 1) : nKt;
 
-  for (int c = tid; c < TQ * D / 8; c += kThreads) {
-    const int r = c / (D / 8), col = (c % (D / 8)) * 8;
-    float tmp[8];
-    if (q0 + r < p.Nq) load8<BF16>(p.q, (qbase + q0 + r) * D + col, tmp);
-    else for (int i = 0; i < 8; ++i) tmp[i] = 0.f;
-    for (int i = 0; i < 8; ++i) Qs[r * S::QS + col + i] = tmp[i];
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(B_KVFULL + s), 1);
+      mbar_init(bar(B_KVEMPTY + s), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(bar(B_S + j), 1);
+      mbar_init(bar(B_P + j), 4);       // one arrival per softmax warp
+      mbar_init(bar(B_SFREE + j), 1);
+    }
+    mbar_init(bar(B_PV), 1);
+    mbar_init(bar(B_AFIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  if (tid < TQ) {
-    row_m[tid] = -CUDART_INF_F;
-    row_l[tid] = 0.f;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
   }
-  constexpr int OC = D / 16;
-  float acc[4][OC];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int c = 0; c < OC; ++c) acc[i][c] = 0.f;
-
-  const int qlast = min(q0 + TQ, p.Nq) - 1;
-  const int kv_end = p.causal ? min(p.Nkv, qlast + 1) : p.Nkv;
-  for (int kv0 = 0; kv0 < kv_end; kv0 += TK) {
-    __syncthreads();
-    for (int c = tid; c < TK * D / 8; c += kThreads) {
-      const int r = c / (D / 8), col = (c % (D / 8)) * 8;
-      float kt[8], vt[8];
-      if (kv0 + r < p.Nkv) {
-        load8<BF16>(p.k, (kbase + kv0 + r) * D + col, kt);
-        load8<BF16>(p.v, (kbase + kv0 + r) * D + col, vt);
-      } else {
-        for (int i = 0; i < 8; ++i) kt[i] = vt[i] = 0.f;
-      }
-      for (int i = 0; i < 8; ++i) {
-        Ks[r * S::KS + col + i] = kt[i];
-        Vs[r * D + col + i] = vt[i];
-      }
-    }
-    __syncthreads();
-    // scores: rows 4ty..4ty+3, columns tx + 16 jj
-    float s[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) s[i][jj] = 0.f;
-    for (int d = 0; d < D; ++d) {
-      float kk[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) kk[jj] = Ks[(tx + 16 * jj) * S::KS + d];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float qv = Qs[(4 * ty + i) * S::QS + d];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) s[i][jj] = fmaf(qv, kk[jj], s[i][jj]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int qi = q0 + 4 * ty + i;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int kj = kv0 + tx + 16 * jj;
-        const bool masked = kj >= p.Nkv || (p.causal && kj > qi);
-        Ss[(4 * ty + i) * S::SS + tx + 16 * jj] = masked ? -CUDART_INF_F : s[i][jj] * p.scale;
-      }
-    }
-    __syncthreads();
-    // running max / sum: 4 threads per row, 16 columns each
-    {
-      const int r = tid / 4, part = tid % 4;
-      float* srow = Ss + r * S::SS + part * 16;
-      float mx = -CUDART_INF_F;
-      for (int c = 0; c < 16; ++c) mx = fmaxf(mx, srow[c]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_old = row_m[r];
-      const float m_new = fmaxf(m_old, mx);
-      float sum = 0.f;
-      for (int c = 0; c < 16; ++c) {
-        const float e = (m_new == -CUDART_INF_F) ? 0.f : expf(srow[c] - m_new);
-        srow[c] = e;
-        sum += e;
-      }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      __syncwarp();
-      if (part == 0) {
-        const float alpha = (m_new == -CUDART_INF_F) ? 1.f : expf(m_old - m_new);
-        row_a[r] = alpha;
-        row_l[r] = row_l[r] * alpha + sum;
-        row_m[r] = m_new;
-      }
-    }
-    __syncthreads();
-    // O = O * alpha + P V ; this thread: rows 4ty+i, columns tx + 16c
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = row_a[4 * ty + i];
-#pragma unroll
-      for (int c = 0; c < OC; ++c) acc[i][c] *= a;
-    }
-    for (int kk = 0; kk < TK; ++kk) {
-      float pv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pv[i] = Ss[(4 * ty + i) * S::SS + kk];
-#pragma unroll
-      for (int c = 0; c < OC; ++c) {
-        const float vv = Vs[kk * D + tx + 16 * c];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][c] = fmaf(pv[i], vv, acc[i][c]);
-      }
-    }
-  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{p.status, abort_flag};
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0 && T > 0) {
+      mbar_arrive_expect_tx(bar(B_Q), L::TILE);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 4 * ty + i;
-    if (q0 + r >= p.Nq) continue;
-    const float inv = 1.f / row_l[r];
-    uint16_t* orow = static_cast<uint16_t*>(p.o) + (qbase + q0 + r) * D;
+      for (int hh = 0; hh < L::NH; ++hh) tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, q0, bh);
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % STAGES;
+        const uint32_t ph = (t / STAGES) & 1;
+        if (t >= STAGES && !mbar_wait(bar(B_KVEMPTY + s), ph ^ 1, wc, 51)) break;
+        const uint32_t fb = bar(B_KVFULL + s);
+        mbar_arrive_expect_tx(fb, 2 * L::TILE);
+        const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
 #pragma unroll
-    for (int c = 0; c < OC; ++c) {
-      const float val = acc[i][c] * inv;
-      uint16_t bits;
-      if constexpr (BF16) {
-        const __nv_bfloat16 t = __float2bfloat16_rn(val);
-        bits = *reinterpret_cast<const uint16_t*>(&t);
-      } else {
-        const __half t = __float2half_rn(val);
-        bits = *reinterpret_cast<const uint16_t*>(&t);
+        for (int hh = 0; hh < L::NH; ++hh) {
+          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, t * BK, kvh);
+          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, t * BK, kvh);
+        }
+        issued = t + 1;
       }
-      orow[tx + 16 * c] = bits;
+      drain_wait(bar(B_Q), 0);
+      for (int t = max(0, issued - STAGES); t < issued; ++t)
+        drain_wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1);
     }
+  } else if (warp == 1 || warp == 2) {
+    // ================================================================ MMA issuers
+    if (T > 0) {
+      constexpr uint32_t ID_S = make_idesc_f16(128, BK, BF16, false, false);
+      constexpr uint32_t ID_O = make_idesc_f16(128, D, BF16, false, true);
+      const uint32_t tO = tmem + L::COL_O;
+      const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q, 16, 1024);
+      auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BK; };
+      auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_KV + (t % STAGES) * 2 * L::TILE; };
+      auto kstep = [](int ks) -> uint64_t {
+        return static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
+      };
+      auto wait = [&](uint32_t bb, uint32_t parity, uint32_t site) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bb, parity, wc, site));
+      };
+      if (warp == 1) {
+        bool ok = wait(bar(B_Q), 0, 52);
+        for (int t = 0; ok && t < T; ++t) {
+          // G1: S = Q K^T into buffer t & 1, once PV(t-2) has read the P that was there
+          if (!wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1, 53)) break;
+          if (t >= 2 && !wait(bar(B_SFREE + (t & 1)), ((t - 2) >> 1) & 1, 54)) break;
+          tc_fence_after();
+          const uint64_t dK_k = sw128_desc(k_tile(t), 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) umma_ss_warp(s_buf(t), dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
+          umma_commit_warp(bar(B_S + (t & 1)));
+        }
+        umma_commit_warp(bar(B_AFIN));
+        drain_wait(bar(B_AFIN), 0);
+      } else {
+        for (int t = 0; t < T; ++t) {
+          // PV: O += P V  (P, 16-bit, packed into the first half of its S buffer; V read MN-major)
+          if (!wait(bar(B_P + (t & 1)), (t >> 1) & 1, 55)) break;
+          tc_fence_after();
+          const uint64_t dV_mn = sw128_desc(k_tile(t) + L::TILE, L::HALF, 1024);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_ts_warp(tO, s_buf(t) + 8 * ks, dV_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_O,
+                         (t > 0 || ks > 0));
+          umma_commit_warp(bar(B_SFREE + (t & 1)));
+          umma_commit_warp(bar(B_PV));
+          umma_commit_warp(bar(B_KVEMPTY + t % STAGES));   // G1(t) completed before P(t) existed
+        }
+        if (*abort_flag) drain_wait(bar(B_PV), (T - 1) & 1);
+      }
+    }
+  } else if (warp >= 4) {
+    // ================================================================ softmax group
+    const int r = threadIdx.x - 128;                    // query row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tO = tmem + lane_off + L::COL_O;
+    const int q = q0 + r;
+    float m_ref = 0.f;                                  // reference max (log2 units)
+    float l = 0.f;                                      // sum of 2^(x - m_ref)
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int kv0 = t * BK;
+      // columns c >= lim are masked: past the end of K/V, or (causal) after query q
+      int lim = p.Nkv - kv0;
+      if (p.causal) lim = min(lim, q - kv0 + 1);
+      const bool need_mask = __any_sync(0xffffffffu, lim < BK);
+      const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 56))) { ok = false; break; }
+      tc_fence_after();
+      float x[BK];
+#pragma unroll
+      for (int ch = 0; ch < BK / 32; ++ch) {
+        uint32_t sr[32];
+        tmem_ld_x32(tS + 32 * ch, sr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[32 * ch + c] = __uint_as_float(sr[c]) * p.scale_log2;
+      }
+      float mt = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < BK; ++c) {
+        if (need_mask && c >= lim) x[c] = -CUDART_INF_F;
+        mt = fmaxf(mt, x[c]);
+      }
+      if (t == 0) {
+        m_ref = (mt == -CUDART_INF_F) ? 0.f : mt;
+      } else {
+        // Move the reference max only when P would exceed 2^8; then O and the sum are
+        // rescaled, which needs the previous P V to have completed.
+        const bool resc = mt > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, resc)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV), (t - 1) & 1, wc, 57))) { ok = false; break; }
+          tc_fence_after();
+          const float alpha = resc ? ex2_approx(m_ref - mt) : 1.f;
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t ov[32];
+            tmem_ld_x32(tO + 32 * ch, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st_x32(tO + 32 * ch, ov);
+          }
+          tmem_st_wait();
+          if (resc) {
+            l *= alpha;
+            m_ref = mt;
+          }
+        }
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < BK / 32; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const float p0 = ex2_approx(x[32 * ch + 2 * c2] - m_ref);
+          const float p1 = ex2_approx(x[32 * ch + 2 * c2 + 1] - m_ref);
+          lsum += p0 + p1;
+          pk[c2] = pack2<BF16>(p0, p1);
+        }
+        // columns [16ch, 16ch+16) of S were already read
+        tmem_st_x16(tS + 16 * ch, pk);
+      }
+      l += lsum;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P + (t & 1)));
+    }
+    // ---- epilogue: O = acc / l (16-bit), L = (m_ref + log2 l) * ln 2
+    bool have = ok && T > 0;
+    if (have) {
+      have = __all_sync(0xffffffffu, mbar_wait(bar(B_PV), (T - 1) & 1, wc, 58));
+      tc_fence_after();
+    }
+    const bool aborted = *abort_flag != 0;
+    const float inv = 1.f / l;
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + q) * D * 2;
+#pragma unroll 1
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t pk[16];
+      if (have) {
+        uint32_t v[32];
+        tmem_ld_x32(tO + 32 * ch, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack2<BF16>(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = 0u;
+      }
+      if (q < p.Nq && !aborted) {
+        uint4* d4 = reinterpret_cast<uint4*>(out + ch * 64);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+      }
+    }
+    if (q < p.Nq && !aborted) p.lse[static_cast<size_t>(bh) * p.Nq + q] = (m_ref + __log2f(l)) * 0.69314718055994531f;
   }
-  if (tid < TQ && q0 + tid < p.Nq) p.lse[qbase + q0 + tid] = row_m[tid] + logf(row_l[tid]);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 template <int D, bool BF16>
-cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
-  using S = Smem<D>;
+cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     unsigned int* status, cudaStream_t stream) {
+  using L = Layout<D>;
   auto kern = fwd_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  Params p{a.q, a.k, a.v, a.o, a.lse, a.pb.B, a.pb.Hq, a.pb.Hkv, a.pb.Nq, a.pb.Nkv, a.pb.scale, a.pb.causal};
-  dim3 grid((a.pb.Nq + TQ - 1) / TQ, a.pb.Hq, a.pb.B);
-  kern<<<grid, kThreads, S::BYTES, stream>>>(p);
+  Params p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.status = status;
+  p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv;
+  p.scale_log2 = a.pb.scale * 1.4426950408889634f;
+  p.causal = a.pb.causal;
+  const long long grid = static_cast<long long>((a.pb.Nq + BQ - 1) / BQ) * a.pb.B * a.pb.Hq;
+  kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.pb.d == 128) return a.pb.bf16 ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
-  return a.pb.bf16 ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       unsigned int* status, cudaStream_t stream) {
+  if (a.pb.d == 128)
+    return a.pb.bf16 ? launch_t<128, true>(a, tq, tk, tv, status, stream)
+                     : launch_t<128, false>(a, tq, tk, tv, status, stream);
+  return a.pb.bf16 ? launch_t<64, true>(a, tq, tk, tv, status, stream)
+                   : launch_t<64, false>(a, tq, tk, tv, status, stream);
 }
 
 }  // namespace fa

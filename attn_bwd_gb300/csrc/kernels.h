@@ -68,7 +68,8 @@ cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUte
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
-// fwd.cu
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+// fwd.cu: maps are Q, K, V (box 64 x 128 rows)
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       unsigned int* status, cudaStream_t stream);
 
 }  // namespace fa
