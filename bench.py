@@ -283,6 +283,19 @@ def main():
     peak = float(peaks["bf16_tflops"])
     traffic = traffic_per_launch(sh, det)
 
+    # ---- the forward that makes O and L (not part of the step): timed separately, same roofline
+    fwd_iters = 10
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(fwd_iters):
+        st = _lib.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, N, d, scale, causal, dt_code, stream)
+        if st:
+            raise RuntimeError(f"fa_fwd failed: {st}")
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = f0.elapsed_time(f1) / fwd_iters
+    fwd_flops = 4.0 * B * Hq * N * N * d / (2 if causal else 1)
+
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
@@ -330,6 +343,10 @@ def main():
                       "other_avg": ms_total / args.steps - main_avg},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
+        "forward": {"kernel": "fwd_kernel (makes O and L; outside the timed step)", "ms": fwd_ms,
+                    "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
+                    "frac": fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak,
+                    "flops": "4*B*Hq*Nq*Nkv*d, halved for causal"},
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
