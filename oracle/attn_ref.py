@@ -12,12 +12,20 @@ h_kv = h // (Hq // Hkv), i.e. consecutive groups of query heads share one
 key/value head -- the plainest reading of the GQA support described in
 "[Kernel] Flash attention 2" (Liger-Kernel #275), "Details"):
 
-  S_ij  = scale * sum_c Q_ic K_jc, and S_ij = -inf when causal and j > i
+  S_ij  = scale * sum_c Q_ic K_jc, and S_ij = -inf when causal and j > i + delta
           (flash_attention_backward.cu, rustytorch rtx-flash-attention,
-          blocks "Recompute attention scores" and "Apply causal mask")
+          blocks "Recompute attention scores" and "Apply causal mask", where
+          delta = 0: the top-left alignment).  "[Kernel] Flash attention 2"
+          (Liger-Kernel #275, "Details") lists causal masking together with
+          different Q and KV lengths without fixing the alignment; the second
+          option here, bottom-right, takes delta = Nkv - Nq so that the last
+          query sees every key.  With Nq > Nkv its first Nq - Nkv rows see no
+          key at all.
   L_i   = log sum_j exp(S_ij)         natural log of the *scaled* scores
-          (same file, block "Compute softmax probabilities from scores and LSE")
-  P_ij  = exp(S_ij - L_i)             (same block)
+          (same file, block "Compute softmax probabilities from scores and LSE");
+          -inf for a row that sees no key (the log of an empty sum)
+  P_ij  = exp(S_ij - L_i)             (same block); 0 wherever S_ij = -inf, so a
+          row that sees no key has P = 0, O = 0, dS = 0 and dQ = 0
   O_i   = sum_j P_ij V_j
   dV_j  = sum_i P_ij dO_i             (same file, block "Compute dV")
   dP_ij = sum_c dO_ic V_jc            (same file, block "Compute dS", first step)
@@ -53,32 +61,67 @@ def kv_head(h: int, Hq: int, Hkv: int) -> int:
     return h // (Hq // Hkv)
 
 
-def scores(q: np.ndarray, k: np.ndarray, scale: float, causal: bool) -> np.ndarray:
-    """S = scale * Q K^T for one head, [Nq, Nkv], with the top-left causal mask.
+# Values of the ``causal`` argument (the same numbers the C interface takes;
+# ``False`` / ``True`` mean none / top-left).
+CAUSAL_NONE = 0
+CAUSAL_TOP_LEFT = 1
+CAUSAL_BOTTOM_RIGHT = 2
 
-    Causal masking drops key j for query i whenever j > i (the literal rule
-    of the pages' CUDA kernel); with Nq == Nkv this is the usual mask.
+
+def causal_delta(causal, nq: int, nk: int):
+    """delta of the mask rule "key j masked for query i when j > i + delta", or None (no mask)."""
+    c = int(causal)
+    if c == CAUSAL_NONE:
+        return None
+    if c == CAUSAL_TOP_LEFT:
+        return 0
+    if c == CAUSAL_BOTTOM_RIGHT:
+        return nk - nq
+    raise ValueError(f"unknown causal mode {causal!r}")
+
+
+def scores(q: np.ndarray, k: np.ndarray, scale: float, causal) -> np.ndarray:
+    """S = scale * Q K^T for one head, [Nq, Nkv], with the causal mask applied.
+
+    Top-left drops key j for query i whenever j > i (the literal rule of the
+    pages' CUDA kernel); bottom-right whenever j > i + Nkv - Nq.  With
+    Nq == Nkv both are the usual mask.
     """
     s = scale * (q @ k.T)
-    if causal:
-        nq, nk = s.shape
+    nq, nk = s.shape
+    delta = causal_delta(causal, nq, nk)
+    if delta is not None:
         i = np.arange(nq)[:, None]
         j = np.arange(nk)[None, :]
-        s = np.where(j > i, -np.inf, s)
+        s = np.where(j > i + delta, -np.inf, s)
     return s
 
 
 def logsumexp_rows(s: np.ndarray) -> np.ndarray:
-    """L_i = log sum_j exp(S_ij), evaluated stably as m_i + log sum_j exp(S_ij - m_i)."""
+    """L_i = log sum_j exp(S_ij), evaluated stably as m_i + log sum_j exp(S_ij - m_i).
+
+    A row whose scores are all -inf (it sees no key) gets -inf.
+    """
     m = s.max(axis=1)
-    return m + np.log(np.exp(s - m[:, None]).sum(axis=1))
+    out = np.full(s.shape[0], -np.inf)
+    seen = np.isfinite(m)
+    out[seen] = m[seen] + np.log(np.exp(s[seen] - m[seen, None]).sum(axis=1))
+    return out
+
+
+def probs(s: np.ndarray, lse: np.ndarray) -> np.ndarray:
+    """P_ij = exp(S_ij - L_i), and exactly 0 where S_ij = -inf (masked)."""
+    p = np.zeros_like(s)
+    live = np.isfinite(s)
+    p[live] = np.exp(s[live] - np.broadcast_to(lse[:, None], s.shape)[live])
+    return p
 
 
 def head_forward(q, k, v, scale, causal):
     """Forward for one head: returns (O [Nq,d], L [Nq], P [Nq,Nkv])."""
     s = scores(q, k, scale, causal)
     lse = logsumexp_rows(s)
-    p = np.exp(s - lse[:, None])
+    p = probs(s, lse)
     return p @ v, lse, p
 
 
@@ -96,7 +139,7 @@ def head_backward(q, k, v, do, scale, causal, lse=None, o=None):
     s = scores(q, k, scale, causal)
     if lse is None:
         lse = logsumexp_rows(s)
-    p = np.exp(s - lse[:, None])
+    p = probs(s, lse)
     if o is None:
         o = p @ v
     dv = p.T @ do

@@ -100,6 +100,9 @@ FD_CASES = [
     (1, 2, 1, 3, 5, 2, True),     # Nq != Nkv, top-left causal
     (1, 4, 2, 4, 3, 2, False),    # GQA with two kv heads
     (2, 2, 2, 2, 3, 2, True),
+    (1, 2, 1, 3, 5, 2, 2),        # bottom-right causal, Nq < Nkv
+    (1, 2, 1, 5, 3, 2, 2),        # bottom-right causal, Nq > Nkv: two rows see no key
+    (1, 4, 2, 4, 4, 2, 2),        # bottom-right causal, Nq == Nkv
 ]
 
 
@@ -291,3 +294,104 @@ def test_golden_regression_record():
         np.testing.assert_allclose(lse, c["lse"], rtol=0, atol=1e-15)
         for n in ("dq", "dk", "dv", "D"):
             np.testing.assert_allclose(g[n], c[n], rtol=0, atol=1e-15)
+
+
+# ------------------------------------------------------ causal alignment
+
+BR = attn_ref.CAUSAL_BOTTOM_RIGHT
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,d", [
+    (1, 2, 1, 17, 31, 8),
+    (2, 4, 2, 5, 40, 8),
+    (1, 2, 2, 24, 24, 8),
+])
+def test_bottom_right_matches_torch_sdpa_with_explicit_mask(B, Hq, Hkv, Nq, Nkv, d):
+    """Nq <= Nkv: every row sees a key, so torch's fp64 SDPA with the explicit
+    bottom-right boolean mask (key j allowed for query i iff j <= i + Nkv - Nq)
+    is an independent derivation of O, L and the gradients."""
+    g = torch.Generator().manual_seed(23)
+    q = torch.randn(B, Hq, Nq, d, generator=g, dtype=torch.float64)
+    k = torch.randn(B, Hkv, Nkv, d, generator=g, dtype=torch.float64)
+    v = torch.randn(B, Hkv, Nkv, d, generator=g, dtype=torch.float64)
+    do = torch.randn(B, Hq, Nq, d, generator=g, dtype=torch.float64)
+    scale = 0.4
+    allowed = torch.ones(Nq, Nkv, dtype=torch.bool).tril(diagonal=Nkv - Nq)
+    tq, tk, tv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    rep = Hq // Hkv
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(rep, dim=1), tv.repeat_interleave(rep, dim=1), attn_mask=allowed, scale=scale)
+    out.backward(do)
+    logits = scale * (q @ k.repeat_interleave(rep, dim=1).transpose(-1, -2))
+    lse_t = torch.logsumexp(logits.masked_fill(~allowed, float("-inf")), dim=-1)
+    o, lse = attn_ref.forward(q, k, v, scale, BR)
+    r = attn_ref.backward(q, k, v, do, scale, BR)
+    np.testing.assert_allclose(o, out.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dq"], tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dk"], tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dv"], tv.grad.numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(7, 3), (12, 5), (4, 1)])
+def test_bottom_right_with_more_queries_reduces_to_top_left(Nq, Nkv):
+    """Nq > Nkv: the first m = Nq - Nkv rows see no key (O = 0, L = -inf, dQ = 0),
+    and the rest is the top-left problem of the last Nkv queries, whose dK, dV
+    are the whole problem's."""
+    rng = np.random.default_rng(Nq * 100 + Nkv)
+    q, do = _rand((1, 2, Nq, 4), rng), _rand((1, 2, Nq, 4), rng)
+    k, v = _rand((1, 1, Nkv, 4), rng), _rand((1, 1, Nkv, 4), rng)
+    m = Nq - Nkv
+    o, lse = attn_ref.forward(q, k, v, 0.6, BR)
+    r = attn_ref.backward(q, k, v, do, 0.6, BR)
+    o_tl, lse_tl = attn_ref.forward(q[:, :, m:], k, v, 0.6, True)
+    r_tl = attn_ref.backward(q[:, :, m:], k, v, do[:, :, m:], 0.6, True)
+    assert (o[:, :, :m] == 0).all() and np.isneginf(lse[:, :, :m]).all()
+    assert (r["dq"][:, :, :m] == 0).all() and (r["D"][:, :, :m] == 0).all()
+    np.testing.assert_allclose(o[:, :, m:], o_tl, atol=1e-14)
+    np.testing.assert_allclose(lse[:, :, m:], lse_tl, atol=1e-14)
+    for n in ("dq",):
+        np.testing.assert_allclose(r[n][:, :, m:], r_tl[n], atol=1e-14)
+    for n in ("dk", "dv"):
+        np.testing.assert_allclose(r[n], r_tl[n], atol=1e-14)
+
+
+def test_bottom_right_single_key_closed_form():
+    """Nq=3, Nkv=1, bottom-right: rows 0, 1 see nothing; row 2 sees the one key,
+    so P = 1 there: O_2 = V_0, L_2 = S_20, dV_0 = dO_2, and dS = 0 gives dQ = dK = 0."""
+    rng = np.random.default_rng(3)
+    q, do = _rand((1, 1, 3, 2), rng), _rand((1, 1, 3, 2), rng)
+    k, v = _rand((1, 1, 1, 2), rng), _rand((1, 1, 1, 2), rng)
+    o, lse = attn_ref.forward(q, k, v, 0.5, BR)
+    r = attn_ref.backward(q, k, v, do, 0.5, BR)
+    np.testing.assert_array_equal(o[0, 0, :2], 0.0)
+    np.testing.assert_allclose(o[0, 0, 2], v[0, 0, 0], atol=1e-15)
+    assert np.isneginf(lse[0, 0, :2]).all()
+    assert lse[0, 0, 2] == pytest.approx(0.5 * q[0, 0, 2] @ k[0, 0, 0], abs=1e-15)
+    np.testing.assert_allclose(r["dv"][0, 0, 0], do[0, 0, 2], atol=1e-15)
+    np.testing.assert_array_equal(r["dq"], 0.0)
+    np.testing.assert_array_equal(r["dk"], 0.0)
+
+
+def test_alignments_agree_when_lengths_are_equal():
+    rng = np.random.default_rng(8)
+    q, do = _rand((1, 2, 9, 4), rng), _rand((1, 2, 9, 4), rng)
+    k, v = _rand((1, 1, 9, 4), rng), _rand((1, 1, 9, 4), rng)
+    a = attn_ref.backward(q, k, v, do, 0.5, True)
+    b = attn_ref.backward(q, k, v, do, 0.5, BR)
+    for n in ("dq", "dk", "dv", "D"):
+        np.testing.assert_array_equal(a[n], b[n])
+
+
+def test_unknown_causal_mode_is_rejected():
+    with pytest.raises(ValueError):
+        attn_ref.causal_delta(3, 4, 4)
+
+
+def test_pins_catch_wrong_bottom_right_offset(monkeypatch):
+    src = inspect.getsource(attn_ref.causal_delta)
+    ns = dict(attn_ref.__dict__)
+    exec(src.replace("return nk - nq", "return nq - nk"), ns)
+    monkeypatch.setattr(attn_ref, "causal_delta", ns["causal_delta"])
+    with pytest.raises(AssertionError):
+        test_bottom_right_matches_torch_sdpa_with_explicit_mask(1, 2, 1, 17, 31, 8)
