@@ -28,6 +28,9 @@ FA_ERR_DEVICE_TIMEOUT = 9
 FA_ERR_ARG = 10
 FA_F16 = 0
 FA_BF16 = 1
+FA_CAUSAL_NONE = 0
+FA_CAUSAL_TOP_LEFT = 1
+FA_CAUSAL_BOTTOM_RIGHT = 2
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

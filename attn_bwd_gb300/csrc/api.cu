@@ -110,7 +110,8 @@ Problem make_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale
   pb.B = B; pb.Hq = Hq; pb.Hkv = Hkv; pb.Nq = Nq; pb.Nkv = Nkv; pb.d = d;
   pb.NqPad = round_up(Nq, kRowPad);
   pb.scale = scale;
-  pb.causal = causal ? 1 : 0;
+  pb.causal = causal != FA_CAUSAL_NONE ? 1 : 0;
+  pb.causal_off = causal == FA_CAUSAL_BOTTOM_RIGHT ? Nkv - Nq : 0;
   pb.bf16 = dtype == FA_BF16 ? 1 : 0;
   pb.deterministic = deterministic ? 1 : 0;
   return pb;
@@ -160,7 +161,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
   if (st) return st;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(lse)) return FA_ERR_ALIGN;
-  if (!std::isfinite(scale)) return FA_ERR_ARG;
+  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
   FwdArgs a;
   a.pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, 1);
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
@@ -196,7 +197,7 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, voi
   if (st) return st;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dO) || misaligned(dk) || misaligned(dv))
     return FA_ERR_ALIGN;
-  if (!std::isfinite(scale)) return FA_ERR_ARG;
+  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
   if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
   if ((st = get_encoder())) return st;
   MainArgs a;
@@ -221,7 +222,7 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void*
   int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
   if (st) return st;
   if (misaligned(dq)) return FA_ERR_ALIGN;
-  if (!std::isfinite(scale)) return FA_ERR_ARG;
+  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
   if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
   DqArgs a;
   a.pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic);
@@ -250,7 +251,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(dO) || misaligned(lse) ||
       misaligned(dq) || misaligned(dk) || misaligned(dv))
     return FA_ERR_ALIGN;
-  if (!std::isfinite(scale)) return FA_ERR_ARG;
+  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
   if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
   if ((st = fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, Nq, Nkv, d, dtype, deterministic, workspace, workspace_bytes,
                               stream)))

@@ -71,7 +71,7 @@ struct Params {
   unsigned int* status;
   int B, Hq, Hkv, Nq, Nkv, NqPad;
   float scale, scale_log2;
-  int causal;
+  int causal, causal_off;
 };
 
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -110,7 +110,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int q0 = i * BQ;
   const int nKt = (p.Nkv + BK - 1) / BK;
   const int qmax = min(q0 + BQ, p.Nq) - 1;
-  const int T = p.causal ? min(nKt, qmax / BK + 1) : nKt;
+  // causal: the last key any row of this tile sees is qmax + causal_off (none if negative)
+  const int kmax = qmax + p.causal_off;
+  const int T = p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
@@ -245,7 +247,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int kv0 = t * BK;
       // columns c >= lim are masked: past the end of K/V, or (causal) after query q
       int lim = p.Nkv - kv0 - 64 * grp;
-      if (p.causal) lim = min(lim, q - kv0 - 64 * grp + 1);
+      if (p.causal) lim = min(lim, q + p.causal_off - kv0 - 64 * grp + 1);
       const bool need_mask = __any_sync(0xffffffffu, lim < 64);
       const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK + 64 * grp;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 28))) break;
@@ -341,6 +343,7 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
   p.scale = a.pb.scale;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
+  p.causal_off = a.pb.causal_off;
   const long long grid = static_cast<long long>((a.pb.Nq + BQ - 1) / BQ) * a.pb.B * a.pb.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();

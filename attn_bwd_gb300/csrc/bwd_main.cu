@@ -108,7 +108,7 @@ struct Params {
   unsigned int* status;
   int B, Hq, Hkv, Nq, Nkv, NqPad;
   float scale, scale_log2;
-  int causal;
+  int causal, causal_off;
 };
 
 // Bounded wait that ignores the abort flag: used only to drain work already
@@ -156,7 +156,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int G = p.Hq / p.Hkv;
   const int kv0 = j * BN;
   const int nQt = (p.Nq + BM - 1) / BM;
-  const int i0 = p.causal ? min(kv0 / BM, nQt) : 0;   // first query tile that sees this KV tile
+  // first query tile that sees this KV tile: causal, query q sees key kv0 when q >= kv0 - causal_off
+  const int qfirst = kv0 - p.causal_off;
+  const int i0 = p.causal ? (qfirst <= 0 ? 0 : min(qfirst / BM, nQt)) : 0;
   const int per_head = nQt - i0;
   const int T = G * per_head;                          // tiles this CTA processes
 
@@ -356,7 +358,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // columns c < lim are masked: key kv lies after query q0 + 32 grp + c.
       // Only KV-tail rows and the diagonal tiles need the per-element test;
       // the decision is made once per warp.
-      const int lim = p.causal ? (kv - q0 - 32 * grp) : INT_MIN;
+      const int lim = p.causal ? (kv - p.causal_off - q0 - 32 * grp) : INT_MIN;
       const bool need_mask = __any_sync(0xffffffffu, !row_ok || lim > 0);
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 7))) break;
       tc_fence_after();
@@ -527,6 +529,7 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   p.scale = a.pb.scale;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
+  p.causal_off = a.pb.causal_off;
   const long long nkt = (a.pb.Nkv + BN - 1) / BN;
   const long long grid = nkt * a.pb.B * a.pb.Hkv;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);

@@ -66,7 +66,7 @@ struct Params {
   unsigned int* status;
   int B, Hq, Hkv, Nq, Nkv;
   float scale_log2;
-  int causal;
+  int causal, causal_off;
 };
 
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -104,7 +104,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   const int q0 = i * BQ;
   const int nKt = (p.Nkv + BK - 1) / BK;
   const int qmax = min(q0 + BQ, p.Nq) - 1;
-  const int T = p.causal ? min(nKt, qmax / BK + 1) : nKt;
+  // causal: the last key any row of this tile sees is qmax + causal_off (none if negative)
+  const int kmax = qmax + p.causal_off;
+  const int T = p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
@@ -216,7 +218,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int kv0 = t * BK;
       // columns c >= lim are masked: past the end of K/V, or (causal) after query q
       int lim = p.Nkv - kv0;
-      if (p.causal) lim = min(lim, q - kv0 + 1);
+      if (p.causal) lim = min(lim, q + p.causal_off - kv0 + 1);
       const bool need_mask = __any_sync(0xffffffffu, lim < BK);
       const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 56))) { ok = false; break; }
@@ -289,7 +291,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
-    const float inv = 1.f / l;
+    const float inv = l > 0.f ? 1.f / l : 0.f;         // a row that saw no key: O = 0
     uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + q) * D * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
@@ -311,7 +313,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
       }
     }
-    if (q < p.Nq && !aborted) p.lse[static_cast<size_t>(bh) * p.Nq + q] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+    if (q < p.Nq && !aborted)
+      p.lse[static_cast<size_t>(bh) * p.Nq + q] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
   }
 
   tc_fence_before();
@@ -336,6 +339,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
+  p.causal_off = a.pb.causal_off;
   const long long grid = static_cast<long long>((a.pb.Nq + BQ - 1) / BQ) * a.pb.B * a.pb.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -26,6 +26,7 @@ struct Problem {
   int NqPad;
   float scale;
   int causal;
+  int causal_off;   // key j is masked for query i when causal and j > i + causal_off
   int bf16;
   int deterministic;
 };

@@ -33,7 +33,7 @@ class Shape:
     Nq: int
     Nkv: int
     d: int
-    causal: bool
+    causal: int                  # 0 / False: none, 1 / True: top-left, 2: bottom-right
     dtype: str = "bf16"          # "f16" or "bf16"
     dist: str = "normal"         # "normal" -> N(0,1), "uniform" -> U[0,1)
     scale: float | None = None   # None -> 1/sqrt(d)
@@ -47,7 +47,7 @@ class Shape:
         return DTYPES[self.dtype]
 
     def name(self) -> str:
-        c = "causal" if self.causal else "full"
+        c = {0: "full", 1: "causal", 2: "causalbr"}[int(self.causal)]
         return (f"B{self.B}_Hq{self.Hq}_Hkv{self.Hkv}_Nq{self.Nq}_Nkv{self.Nkv}"
                 f"_d{self.d}_{self.dtype}_{self.dist}_{c}")
 

@@ -37,8 +37,11 @@ def _need(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
-def forward(q, k, v, scale: float, causal: bool, stream=None):
-    """Returns (O, L): O like q, L fp32 [B, Hq, Nq] (natural-log LSE of the scaled scores)."""
+def forward(q, k, v, scale: float, causal, stream=None):
+    """Returns (O, L): O like q, L fp32 [B, Hq, Nq] (natural-log LSE of the scaled scores).
+
+    ``causal``: False / True (top-left) or one of _lib.FA_CAUSAL_* (2 = bottom-right).
+    """
     _need(q, k, v)
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     o = torch.empty_like(q)
@@ -56,7 +59,7 @@ def workspace(q, k, deterministic: bool) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
-def backward(q, k, v, o, do, lse, scale: float, causal: bool, deterministic: bool = False, ws=None,
+def backward(q, k, v, o, do, lse, scale: float, causal, deterministic: bool = False, ws=None,
              out=None, stream=None):
     """Returns (dQ, dK, dV), freshly written (never accumulated)."""
     _need(q, k, v, o, do, lse)

@@ -4,9 +4,12 @@
  * What is computed (per batch b and query head h; key/value head
  * h_kv = h / (Hq / Hkv), consecutive query heads share one key/value head):
  *
- *   S = scale * Q K^T, causal: S[i][j] = -inf when j > i  (top-left)
- *   L = logsumexp_j S       (natural log of the scaled scores)
- *   P = exp(S - L),  O = P V
+ *   S = scale * Q K^T, causal: S[i][j] = -inf when j > i + delta, where
+ *       delta = 0 (causal = FA_CAUSAL_TOP_LEFT) or Nkv - Nq (FA_CAUSAL_BOTTOM_RIGHT)
+ *   L = logsumexp_j S       (natural log of the scaled scores; -inf for a row
+ *                            that sees no key, which bottom-right gives the
+ *                            first Nq - Nkv rows when Nq > Nkv)
+ *   P = exp(S - L) (0 where S = -inf),  O = P V
  *   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO o O),  dS = P o (dP - D)
  *   dQ = scale * dS K,  dK = scale * dS^T Q
  *   dK, dV of a key/value head are summed over the query heads of its group.
@@ -56,10 +59,23 @@ typedef enum {
   FA_ERR_DTYPE = 7,           /* dtype not an fa_dtype value                        */
   FA_ERR_CUDA = 8,            /* a CUDA launch or driver call failed                */
   FA_ERR_DEVICE_TIMEOUT = 9,  /* a bounded device-side wait ran out (see fa_last_device_error) */
-  FA_ERR_ARG = 10             /* another argument is out of range (scale not finite, ...) */
+  FA_ERR_ARG = 10             /* another argument is out of range (scale not finite, causal unknown, ...) */
 } fa_status;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/*
+ * Values of every entry point's `causal` argument.  The source kernel masks
+ * key j for query i when j > i (top-left); "[Kernel] Flash attention 2"
+ * (Liger-Kernel #275, "Details") lists causal masking together with different
+ * Q and KV lengths without fixing the alignment, so both are offered.  With
+ * Nq == Nkv they coincide.  Any other value is FA_ERR_ARG.
+ */
+typedef enum {
+  FA_CAUSAL_NONE = 0,
+  FA_CAUSAL_TOP_LEFT = 1,      /* key j masked for query i when j > i             */
+  FA_CAUSAL_BOTTOM_RIGHT = 2   /* key j masked for query i when j > i + Nkv - Nq  */
+} fa_causal;
 
 /* Largest Nq / Nkv accepted (rows per head). */
 #define FA_MAX_SEQ (1 << 24)

@@ -81,6 +81,8 @@ def _bwd(**kw):
     (dict(workspace_bytes=100), _lib.FA_ERR_WORKSPACE),
     (dict(scale=float("nan"), workspace_bytes=1 << 30), _lib.FA_ERR_ARG),
     (dict(scale=float("inf"), workspace_bytes=1 << 30), _lib.FA_ERR_ARG),
+    (dict(causal=3, workspace_bytes=1 << 30), _lib.FA_ERR_ARG),
+    (dict(causal=-1, workspace_bytes=1 << 30), _lib.FA_ERR_ARG),
 ])
 def test_bwd_rejects_bad_arguments(lib, kw, code):
     assert _bwd(**kw) == code
