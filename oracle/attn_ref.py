@@ -102,6 +102,8 @@ def logsumexp_rows(s: np.ndarray) -> np.ndarray:
 
     A row whose scores are all -inf (it sees no key) gets -inf.
     """
+    if s.shape[1] == 0:
+        return np.full(s.shape[0], -np.inf)
     m = s.max(axis=1)
     out = np.full(s.shape[0], -np.inf)
     seen = np.isfinite(m)
@@ -207,3 +209,61 @@ def backward_flops(B, Hq, Nq, Nkv, d, causal) -> float:
     """FLOPs counted for the backward: 10 * B * Hq * Nq * Nkv * d, halved when causal."""
     f = 10.0 * B * Hq * Nq * Nkv * d
     return f / 2 if causal else f
+
+
+# ------------------------------------------------------------ packed batches
+#
+# Variable-length batches: "[Kernel] Flash attention 2" (Liger-Kernel #275,
+# "Details") supports different Q and KV lengths and places no restriction on
+# the sequence length; a packed batch of sequences of different lengths is the
+# plainest form of that for a batch.  Sequence b occupies rows
+# [cu_q[b], cu_q[b+1]) of every query head of Q [Hq, total_q, d] and rows
+# [cu_k[b], cu_k[b+1]) of every key/value head of K, V [Hkv, total_k, d], and
+# attends only to its own keys, with the causal alignment taken per sequence.
+# The definition is therefore the dense problem above applied to each
+# sequence on its own.
+
+
+def _check_cu(cu, total: int):
+    cu = [int(x) for x in cu]
+    if cu[0] != 0 or cu[-1] != total or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0, not decrease and end at the total")
+    return cu
+
+
+def forward_varlen(q, k, v, cu_q, cu_k, scale: float, causal):
+    """Packed forward: q [Hq, total_q, d], k/v [Hkv, total_k, d].  Returns (O, L) in fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Hq, total_q, d = q.shape
+    Hkv, total_k = k.shape[0], k.shape[1]
+    cu_q, cu_k = _check_cu(cu_q, total_q), _check_cu(cu_k, total_k)
+    o = np.zeros((Hq, total_q, d))
+    lse = np.full((Hq, total_q), -np.inf)
+    for b in range(len(cu_q) - 1):
+        qs, ks = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        for h in range(Hq):
+            hk = kv_head(h, Hq, Hkv)
+            o[h, qs], lse[h, qs], _ = head_forward(q[h, qs], k[hk, ks], v[hk, ks], scale, causal)
+    return o, lse
+
+
+def backward_varlen(q, k, v, do, cu_q, cu_k, scale: float, causal):
+    """Packed backward.  Returns dict of fp64 arrays dq [Hq,total_q,d], dk, dv [Hkv,total_k,d], D."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    Hq, total_q, d = q.shape
+    Hkv, total_k = k.shape[0], k.shape[1]
+    cu_q, cu_k = _check_cu(cu_q, total_q), _check_cu(cu_k, total_k)
+    dq = np.zeros((Hq, total_q, d))
+    dk = np.zeros((Hkv, total_k, d))
+    dv = np.zeros((Hkv, total_k, d))
+    D = np.zeros((Hq, total_q))
+    for b in range(len(cu_q) - 1):
+        qs, ks = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        for h in range(Hq):
+            hk = kv_head(h, Hq, Hkv)
+            r = head_backward(q[h, qs], k[hk, ks], v[hk, ks], do[h, qs], scale, causal)
+            dq[h, qs] = r["dq"]
+            dk[hk, ks] += r["dk"]
+            dv[hk, ks] += r["dv"]
+            D[h, qs] = r["D"]
+    return {"dq": dq, "dk": dk, "dv": dv, "D": D}

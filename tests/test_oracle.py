@@ -395,3 +395,106 @@ def test_pins_catch_wrong_bottom_right_offset(monkeypatch):
     monkeypatch.setattr(attn_ref, "causal_delta", ns["causal_delta"])
     with pytest.raises(AssertionError):
         test_bottom_right_matches_torch_sdpa_with_explicit_mask(1, 2, 1, 17, 31, 8)
+
+
+# ------------------------------------------------------ packed batches
+
+def _pack(x):
+    """[B, H, N, d] -> [H, B*N, d] (sequence b at rows b*N .. b*N + N - 1)."""
+    B, H, N, d = x.shape
+    return np.ascontiguousarray(np.transpose(x, (1, 0, 2, 3)).reshape(H, B * N, d))
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_varlen_equal_lengths_match_dense(causal):
+    rng = np.random.default_rng(40 + causal)
+    B, Hq, Hkv, Nq, Nkv, d = 3, 4, 2, 6, 9, 4
+    q, do = _rand((B, Hq, Nq, d), rng), _rand((B, Hq, Nq, d), rng)
+    k, v = _rand((B, Hkv, Nkv, d), rng), _rand((B, Hkv, Nkv, d), rng)
+    cu_q, cu_k = [b * Nq for b in range(B + 1)], [b * Nkv for b in range(B + 1)]
+    o, lse = attn_ref.forward(q, k, v, 0.5, causal)
+    g = attn_ref.backward(q, k, v, do, 0.5, causal)
+    ov, lv = attn_ref.forward_varlen(_pack(q), _pack(k), _pack(v), cu_q, cu_k, 0.5, causal)
+    gv = attn_ref.backward_varlen(_pack(q), _pack(k), _pack(v), _pack(do), cu_q, cu_k, 0.5, causal)
+    np.testing.assert_allclose(ov, _pack(o), atol=1e-14)
+    np.testing.assert_allclose(lv, np.transpose(lse, (1, 0, 2)).reshape(Hq, B * Nq), atol=1e-14)
+    for n in ("dq", "dk", "dv"):
+        np.testing.assert_allclose(gv[n], _pack(g[n]), atol=1e-14)
+
+
+def _sdpa_packed_mask(cu_q, cu_k, causal):
+    """Allowed-key mask of the whole packed problem: same sequence, and the causal rule in local indices."""
+    tq, tk = cu_q[-1], cu_k[-1]
+    m = np.zeros((tq, tk), dtype=bool)
+    for b in range(len(cu_q) - 1):
+        nq, nk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        i = np.arange(nq)[:, None]
+        j = np.arange(nk)[None, :]
+        delta = {0: None, 1: 0, 2: nk - nq}[causal]
+        ok = np.ones((nq, nk), dtype=bool) if delta is None else (j <= i + delta)
+        m[cu_q[b]:cu_q[b + 1], cu_k[b]:cu_k[b + 1]] = ok
+    return m
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_varlen_matches_torch_sdpa_on_the_packed_sequence(causal):
+    """One packed sequence with a block-diagonal (and per-block causal) mask, through
+    torch's fp64 SDPA and autograd: an independent construction of the packed batch."""
+    lq = [3, 1, 7, 5]
+    lk = [4, 1, 9, 5]                 # nq <= nk everywhere, so every row sees a key
+    cu_q = list(np.cumsum([0] + lq))
+    cu_k = list(np.cumsum([0] + lk))
+    Hq, Hkv, d = 4, 2, 8
+    g = torch.Generator().manual_seed(31 + causal)
+    q = torch.randn(Hq, cu_q[-1], d, generator=g, dtype=torch.float64)
+    k = torch.randn(Hkv, cu_k[-1], d, generator=g, dtype=torch.float64)
+    v = torch.randn(Hkv, cu_k[-1], d, generator=g, dtype=torch.float64)
+    do = torch.randn(Hq, cu_q[-1], d, generator=g, dtype=torch.float64)
+    allowed = torch.from_numpy(_sdpa_packed_mask(cu_q, cu_k, causal))
+    tq, tk, tv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    rep = Hq // Hkv
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq[None], tk.repeat_interleave(rep, dim=0)[None], tv.repeat_interleave(rep, dim=0)[None],
+        attn_mask=allowed, scale=0.35)[0]
+    out.backward(do)
+    o, _ = attn_ref.forward_varlen(q, k, v, cu_q, cu_k, 0.35, causal)
+    r = attn_ref.backward_varlen(q, k, v, do, cu_q, cu_k, 0.35, causal)
+    np.testing.assert_allclose(o, out.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dq"], tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dk"], tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dv"], tv.grad.numpy(), atol=1e-12)
+
+
+def test_varlen_empty_sequences():
+    """A sequence with queries but no keys: O = 0, L = -inf, dQ = 0; a sequence with keys
+    but no queries: dK = dV = 0 for its keys."""
+    rng = np.random.default_rng(9)
+    cu_q, cu_k = [0, 2, 2, 5], [0, 3, 6, 6]     # seq 1: no queries; seq 2: no keys
+    q, do = _rand((2, 5, 4), rng), _rand((2, 5, 4), rng)
+    k, v = _rand((1, 6, 4), rng), _rand((1, 6, 4), rng)
+    for causal in (0, 1, 2):
+        o, lse = attn_ref.forward_varlen(q, k, v, cu_q, cu_k, 0.5, causal)
+        r = attn_ref.backward_varlen(q, k, v, do, cu_q, cu_k, 0.5, causal)
+        assert (o[:, 2:5] == 0).all() and np.isneginf(lse[:, 2:5]).all()
+        assert (r["dq"][:, 2:5] == 0).all()
+        assert (r["dk"][:, 3:6] == 0).all() and (r["dv"][:, 3:6] == 0).all()
+        assert np.isfinite(lse[:, :2]).all()
+
+
+def test_varlen_rejects_inconsistent_offsets():
+    q = np.zeros((1, 4, 2))
+    with pytest.raises(ValueError):
+        attn_ref.forward_varlen(q, q, q, [0, 3, 2, 4], [0, 1, 2, 4], 1.0, 0)
+    with pytest.raises(ValueError):
+        attn_ref.forward_varlen(q, q, q, [0, 2, 3], [0, 2, 4], 1.0, 0)
+
+
+def test_pins_catch_keys_leaking_across_sequences(monkeypatch):
+    for fn in ("forward_varlen", "backward_varlen"):
+        src = inspect.getsource(getattr(attn_ref, fn))
+        assert "slice(cu_k[b], cu_k[b + 1])" in src
+        ns = dict(attn_ref.__dict__)
+        exec(src.replace("slice(cu_k[b], cu_k[b + 1])", "slice(0, cu_k[b + 1])"), ns)
+        monkeypatch.setattr(attn_ref, fn, ns[fn])
+    with pytest.raises(AssertionError):
+        test_varlen_matches_torch_sdpa_on_the_packed_sequence(0)
