@@ -48,6 +48,10 @@ _SIGNATURES = {
     "fa_last_device_error": (_I, [_P]),
     "fa_selftest_wait_timeout": (_I, [_I, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_bwd_varlen_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                           _I, _P, _S, _P]),
 }
 
 FA_STATIC_SCRATCH_BYTES = 64 << 20
@@ -143,3 +147,23 @@ def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scal
     return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, Hq, Hkv, Nq, Nkv, d, float(scale), int(causal), int(dtype),
                                  int(deterministic), _stream(stream))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, B, Hq, Hkv, total_q, total_k, max_q, max_k, d, scale, causal, dtype,
+                  stream=None) -> int:
+    """Packed variable-length forward: q [Hq, total_q, d], k/v [Hkv, total_k, d], cu_* int32 [B + 1] on the device."""
+    return load().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_q), _ptr(cu_k), B, Hq, Hkv,
+                                total_q, total_k, max_q, max_k, d, float(scale), int(causal), int(dtype),
+                                _stream(stream))
+
+
+def fa_bwd_varlen_workspace_size(B, Hq, Hkv, max_q, max_k, d, deterministic) -> int:
+    return load().fa_bwd_varlen_workspace_size(B, Hq, Hkv, max_q, max_k, d, int(deterministic))
+
+
+def fa_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_q, cu_k, B, Hq, Hkv, total_q, total_k, max_q, max_k, d, scale,
+                  causal, dtype, deterministic, workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(cu_q), _ptr(cu_k), B, Hq, Hkv, total_q, total_k, max_q, max_k, d,
+                                float(scale), int(causal), int(dtype), int(deterministic), _ptr(workspace),
+                                int(workspace_bytes), _stream(stream))

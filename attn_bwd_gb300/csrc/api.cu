@@ -104,27 +104,183 @@ Workspace carve(void* ws, int B, int Hq, int Nq, int d, int deterministic) {
   return w;
 }
 
-Problem make_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal, int dtype,
-                     int deterministic) {
+// Where the sequences of a batch live: a dense batch (cu_q == nullptr; Nq, Nkv
+// are the lengths) or a packed one (Nq, Nkv are the longest lengths, total_q,
+// total_k the rows of each head, cu_q / cu_k the device offsets).
+struct Geo {
+  int B, Hq, Hkv, Nq, Nkv, d;
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
+  long long slabs_q() const { return cu_q ? Hq : static_cast<long long>(B) * Hq; }
+  long long slabs_k() const { return cu_q ? Hkv : static_cast<long long>(B) * Hkv; }
+  int rows_q() const { return cu_q ? total_q : Nq; }
+  int rows_k() const { return cu_q ? total_k : Nkv; }
+};
+
+Geo dense(int B, int Hq, int Hkv, int Nq, int Nkv, int d) { return Geo{B, Hq, Hkv, Nq, Nkv, d, nullptr, nullptr, Nq, Nkv}; }
+
+// Largest number of rows per head of a packed batch (keeps every TMA row
+// coordinate, start of a sequence plus a tile, inside int32).
+constexpr int kMaxTotal = 1 << 30;
+
+int check_geo(const Geo& g, int dtype) {
+  int st = check_shape(g.B, g.Hq, g.Hkv, g.Nq, g.Nkv, g.d, dtype);
+  if (st) return st;
+  if (g.cu_q != nullptr || g.cu_k != nullptr) {
+    if (g.cu_q == nullptr || g.cu_k == nullptr) return FA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(g.cu_q) & 3u) || (reinterpret_cast<uintptr_t>(g.cu_k) & 3u)) return FA_ERR_ALIGN;
+    if (g.total_q < 1 || g.total_k < 1 || g.total_q > kMaxTotal || g.total_k > kMaxTotal) return FA_ERR_SHAPE;
+  }
+  return FA_OK;
+}
+
+bool bad_args(float scale, int causal) {
+  return !std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT;
+}
+
+Problem make_problem(const Geo& g, float scale, int causal, int dtype, int deterministic) {
   Problem pb;
-  pb.B = B; pb.Hq = Hq; pb.Hkv = Hkv; pb.Nq = Nq; pb.Nkv = Nkv; pb.d = d;
-  pb.NqPad = round_up(Nq, kRowPad);
+  pb.B = g.B; pb.Hq = g.Hq; pb.Hkv = g.Hkv; pb.Nq = g.Nq; pb.Nkv = g.Nkv; pb.d = g.d;
+  pb.NqPad = round_up(g.Nq, kRowPad);
   pb.scale = scale;
   pb.causal = causal != FA_CAUSAL_NONE ? 1 : 0;
-  pb.causal_off = causal == FA_CAUSAL_BOTTOM_RIGHT ? Nkv - Nq : 0;
+  pb.causal_mode = causal;
+  pb.cu_q = g.cu_q;
+  pb.cu_k = g.cu_k;
+  pb.total_q = g.rows_q();
+  pb.total_k = g.rows_k();
   pb.bf16 = dtype == FA_BF16 ? 1 : 0;
   pb.deterministic = deterministic ? 1 : 0;
   return pb;
 }
 
-int check_ws(void* workspace, size_t bytes, int B, int Hq, int Nq, int d, int deterministic) {
+int check_ws(void* workspace, size_t bytes, const Geo& g, int deterministic) {
   if (workspace == nullptr) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FA_ERR_ALIGN;
-  if (bytes < ws_bytes(B, Hq, Nq, d, deterministic)) return FA_ERR_WORKSPACE;
+  if (bytes < ws_bytes(g.B, g.Hq, g.Nq, g.d, deterministic)) return FA_ERR_WORKSPACE;
   return FA_OK;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+// Tensor maps of the Q-like and K-like tensors of a batch.
+int map_q(CUtensorMap* m, const void* p, int bf, const Geo& g, int box_rows) {
+  return make_map(m, p, bf, g.d, g.rows_q(), g.slabs_q(), box_rows);
+}
+int map_k(CUtensorMap* m, const void* p, int bf, const Geo& g, int box_rows) {
+  return make_map(m, p, bf, g.d, g.rows_k(), g.slabs_k(), box_rows);
+}
+
+int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, float* lse, float scale, int causal,
+            int dtype, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  int st = check_geo(g, dtype);
+  if (st) return st;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(lse)) return FA_ERR_ALIGN;
+  if (bad_args(scale, causal)) return FA_ERR_ARG;
+  FwdArgs a;
+  a.pb = make_problem(g, scale, causal, dtype, 1);
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  if ((st = get_encoder())) return st;
+  unsigned int* status = nullptr;
+  if ((st = status_ptr(&status))) return st;
+  CUtensorMap tq, tk, tv;
+  const int bf = a.pb.bf16;
+  if ((st = map_q(&tq, q, bf, g, 128))) return st;
+  if ((st = map_k(&tk, k, bf, g, 128))) return st;
+  if ((st = map_k(&tv, v, bf, g, 128))) return st;
+  return cuda_status(launch_fwd(a, tq, tk, tv, status, stream));
+}
+
+int run_preprocess(const Geo& g, const void* o, const void* dO, const float* lse, int dtype, int deterministic,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!o || !dO || !lse) return FA_ERR_NULL;
+  int st = check_geo(g, dtype);
+  if (st) return st;
+  if (misaligned(o) || misaligned(dO) || misaligned(lse)) return FA_ERR_ALIGN;
+  if ((st = check_ws(workspace, workspace_bytes, g, deterministic))) return st;
+  unsigned int* status = nullptr;
+  if ((st = status_ptr(&status))) return st;
+  const Problem pb = make_problem(g, 1.0f, 0, dtype, deterministic);
+  const Workspace w = carve(workspace, g.B, g.Hq, g.Nq, g.d, deterministic);
+  return cuda_status(launch_preprocess(pb, o, dO, lse, w, status, stream));
+}
+
+int run_main(const Geo& g, const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+             float scale, int causal, int dtype, int deterministic, void* workspace, size_t workspace_bytes,
+             cudaStream_t stream) {
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_NULL;
+  int st = check_geo(g, dtype);
+  if (st) return st;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dO) || misaligned(dk) || misaligned(dv))
+    return FA_ERR_ALIGN;
+  if (bad_args(scale, causal)) return FA_ERR_ARG;
+  if ((st = check_ws(workspace, workspace_bytes, g, deterministic))) return st;
+  if ((st = get_encoder())) return st;
+  MainArgs a;
+  a.pb = make_problem(g, scale, causal, dtype, deterministic);
+  a.ws = carve(workspace, g.B, g.Hq, g.Nq, g.d, deterministic);
+  a.dk = dk;
+  a.dv = dv;
+  if ((st = status_ptr(&a.status))) return st;
+  CUtensorMap tq, tdo, tk, tv;
+  const int bf = a.pb.bf16;
+  if ((st = map_q(&tq, q, bf, g, 64))) return st;
+  if ((st = map_q(&tdo, dO, bf, g, 64))) return st;
+  if ((st = map_k(&tk, k, bf, g, 128))) return st;
+  if ((st = map_k(&tv, v, bf, g, 128))) return st;
+  return cuda_status(launch_bwd_main(a, tq, tdo, tk, tv, stream));
+}
+
+int run_dq(const Geo& g, const void* q, const void* k, const void* v, const void* dO, void* dq, float scale,
+           int causal, int dtype, int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!dq) return FA_ERR_NULL;
+  int st = check_geo(g, dtype);
+  if (st) return st;
+  if (misaligned(dq)) return FA_ERR_ALIGN;
+  if (bad_args(scale, causal)) return FA_ERR_ARG;
+  if ((st = check_ws(workspace, workspace_bytes, g, deterministic))) return st;
+  DqArgs a;
+  a.pb = make_problem(g, scale, causal, dtype, deterministic);
+  a.ws = carve(workspace, g.B, g.Hq, g.Nq, g.d, deterministic);
+  a.dq = dq;
+  if ((st = status_ptr(&a.status))) return st;
+  if (!deterministic) return cuda_status(launch_dq_convert(a.pb, a.ws, dq, a.status, stream));
+  if (!q || !k || !v || !dO) return FA_ERR_NULL;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dO)) return FA_ERR_ALIGN;
+  if ((st = get_encoder())) return st;
+  CUtensorMap tq, tdo, tk, tv;
+  const int bf = a.pb.bf16;
+  if ((st = map_q(&tq, q, bf, g, 128))) return st;
+  if ((st = map_q(&tdo, dO, bf, g, 128))) return st;
+  if ((st = map_k(&tk, k, bf, g, 128))) return st;
+  if ((st = map_k(&tv, v, bf, g, 128))) return st;
+  return cuda_status(launch_bwd_dq_det(a, tq, tdo, tk, tv, stream));
+}
+
+int run_bwd(const Geo& g, const void* q, const void* k, const void* v, const void* o, const void* dO,
+            const float* lse, void* dq, void* dk, void* dv, float scale, int causal, int dtype, int deterministic,
+            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  int st = check_geo(g, dtype);
+  if (st) return st;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(dO) || misaligned(lse) ||
+      misaligned(dq) || misaligned(dk) || misaligned(dv))
+    return FA_ERR_ALIGN;
+  if (bad_args(scale, causal)) return FA_ERR_ARG;
+  if ((st = check_ws(workspace, workspace_bytes, g, deterministic))) return st;
+  if ((st = run_preprocess(g, o, dO, lse, dtype, deterministic, workspace, workspace_bytes, stream))) return st;
+  if ((st = run_main(g, q, k, v, dO, dk, dv, scale, causal, dtype, deterministic, workspace, workspace_bytes,
+                     stream)))
+    return st;
+  return run_dq(g, q, k, v, dO, dq, scale, causal, dtype, deterministic, workspace, workspace_bytes, stream);
+}
+
+Geo packed(int B, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k, int d, const int* cu_q,
+           const int* cu_k) {
+  return Geo{B, Hq, Hkv, max_q, max_k, d, cu_q, cu_k, total_q, total_k};
+}
 
 }  // namespace
 }  // namespace fa
@@ -157,110 +313,56 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
            int Nkv, int d, float scale, int causal, int dtype, cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
-  int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
-  if (st) return st;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(lse)) return FA_ERR_ALIGN;
-  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
-  FwdArgs a;
-  a.pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, 1);
-  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  if ((st = get_encoder())) return st;
-  unsigned int* status = nullptr;
-  if ((st = status_ptr(&status))) return st;
-  CUtensorMap tq, tk, tv;
-  const int bf = a.pb.bf16;
-  if ((st = make_map(&tq, q, bf, d, Nq, static_cast<long long>(B) * Hq, 128))) return st;
-  if ((st = make_map(&tk, k, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
-  if ((st = make_map(&tv, v, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
-  return cuda_status(launch_fwd(a, tq, tk, tv, status, stream));
+  return run_fwd(dense(B, Hq, Hkv, Nq, Nkv, d), q, k, v, o, lse, scale, causal, dtype, stream);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int Hq, int Hkv, int Nq, int Nkv,
                       int d, int dtype, int deterministic, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream) {
-  if (!o || !dO || !lse) return FA_ERR_NULL;
-  int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
-  if (st) return st;
-  if (misaligned(o) || misaligned(dO) || misaligned(lse)) return FA_ERR_ALIGN;
-  if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
-  const Problem pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, 1.0f, 0, dtype, deterministic);
-  const Workspace w = carve(workspace, B, Hq, Nq, d, deterministic);
-  return cuda_status(launch_preprocess(pb, o, dO, lse, w, stream));
+  return run_preprocess(dense(B, Hq, Hkv, Nq, Nkv, d), o, dO, lse, dtype, deterministic, workspace, workspace_bytes,
+                        stream);
 }
 
 int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq,
                 int Hkv, int Nq, int Nkv, int d, float scale, int causal, int dtype, int deterministic,
                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_NULL;
-  int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
-  if (st) return st;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dO) || misaligned(dk) || misaligned(dv))
-    return FA_ERR_ALIGN;
-  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
-  if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
-  if ((st = get_encoder())) return st;
-  MainArgs a;
-  a.pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic);
-  a.ws = carve(workspace, B, Hq, Nq, d, deterministic);
-  a.dk = dk;
-  a.dv = dv;
-  if ((st = status_ptr(&a.status))) return st;
-  CUtensorMap tq, tdo, tk, tv;
-  const int bf = a.pb.bf16;
-  if ((st = make_map(&tq, q, bf, d, Nq, static_cast<long long>(B) * Hq, 64))) return st;
-  if ((st = make_map(&tdo, dO, bf, d, Nq, static_cast<long long>(B) * Hq, 64))) return st;
-  if ((st = make_map(&tk, k, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
-  if ((st = make_map(&tv, v, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
-  return cuda_status(launch_bwd_main(a, tq, tdo, tk, tv, stream));
+  return run_main(dense(B, Hq, Hkv, Nq, Nkv, d), q, k, v, dO, dk, dv, scale, causal, dtype, deterministic, workspace,
+                  workspace_bytes, stream);
 }
 
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq, int B, int Hq, int Hkv,
               int Nq, int Nkv, int d, float scale, int causal, int dtype, int deterministic, void* workspace,
               size_t workspace_bytes, cudaStream_t stream) {
-  if (!dq) return FA_ERR_NULL;
-  int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
-  if (st) return st;
-  if (misaligned(dq)) return FA_ERR_ALIGN;
-  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
-  if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
-  DqArgs a;
-  a.pb = make_problem(B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic);
-  a.ws = carve(workspace, B, Hq, Nq, d, deterministic);
-  a.dq = dq;
-  if (!deterministic) return cuda_status(launch_dq_convert(a.pb, a.ws, dq, stream));
-  if (!q || !k || !v || !dO) return FA_ERR_NULL;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(dO)) return FA_ERR_ALIGN;
-  if ((st = get_encoder())) return st;
-  if ((st = status_ptr(&a.status))) return st;
-  CUtensorMap tq, tdo, tk, tv;
-  const int bf = a.pb.bf16;
-  if ((st = make_map(&tq, q, bf, d, Nq, static_cast<long long>(B) * Hq, 128))) return st;
-  if ((st = make_map(&tdo, dO, bf, d, Nq, static_cast<long long>(B) * Hq, 128))) return st;
-  if ((st = make_map(&tk, k, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
-  if ((st = make_map(&tv, v, bf, d, Nkv, static_cast<long long>(B) * Hkv, 128))) return st;
-  return cuda_status(launch_bwd_dq_det(a, tq, tdo, tk, tv, stream));
+  return run_dq(dense(B, Hq, Hkv, Nq, Nkv, d), q, k, v, dO, dq, scale, causal, dtype, deterministic, workspace,
+                workspace_bytes, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
            void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal, int dtype,
            int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
-  int st = check_shape(B, Hq, Hkv, Nq, Nkv, d, dtype);
-  if (st) return st;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(dO) || misaligned(lse) ||
-      misaligned(dq) || misaligned(dk) || misaligned(dv))
-    return FA_ERR_ALIGN;
-  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
-  if ((st = check_ws(workspace, workspace_bytes, B, Hq, Nq, d, deterministic))) return st;
-  if ((st = fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, Nq, Nkv, d, dtype, deterministic, workspace, workspace_bytes,
-                              stream)))
-    return st;
-  if ((st = fa_bwd_main(q, k, v, dO, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic, workspace,
-                        workspace_bytes, stream)))
-    return st;
-  return fa_bwd_dq(q, k, v, dO, dq, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic, workspace,
-                   workspace_bytes, stream);
+  return run_bwd(dense(B, Hq, Hkv, Nq, Nkv, d), q, k, v, o, dO, lse, dq, dk, dv, scale, causal, dtype,
+                 deterministic, workspace, workspace_bytes, stream);
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k,
+                  int d, float scale, int causal, int dtype, cudaStream_t stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
+  return run_fwd(packed(B, Hq, Hkv, total_q, total_k, max_q, max_k, d, cu_seqlens_q, cu_seqlens_k), q, k, v, o,
+                 lse, scale, causal, dtype, stream);
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int max_q, int max_k, int d, int deterministic) {
+  return fa_bwd_workspace_size(B, Hq, Hkv, max_q, max_k, d, deterministic);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                  int Hkv, int total_q, int total_k, int max_q, int max_k, int d, float scale, int causal,
+                  int dtype, int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
+  return run_bwd(packed(B, Hq, Hkv, total_q, total_k, max_q, max_k, d, cu_seqlens_q, cu_seqlens_k), q, k, v, o,
+                 dO, lse, dq, dk, dv, scale, causal, dtype, deterministic, workspace, workspace_bytes, stream);
 }
 
 int fa_last_device_error(cudaStream_t stream) {
@@ -272,7 +374,8 @@ int fa_last_device_error(cudaStream_t stream) {
   if (v != 0) {
     const unsigned int zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-    return static_cast<int>(v >> 16) == FA_ERR_DEVICE_TIMEOUT ? FA_ERR_DEVICE_TIMEOUT : FA_ERR_CUDA;
+    const int code = static_cast<int>(v >> 16);
+    return code == FA_ERR_DEVICE_TIMEOUT || code == FA_ERR_ARG ? code : FA_ERR_CUDA;
   }
   return FA_OK;
 }

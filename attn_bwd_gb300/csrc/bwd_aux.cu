@@ -18,6 +18,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -40,7 +41,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
                   float* __restrict__ nLg, float* __restrict__ Dv, float4* __restrict__ dq_acc,
-                  long long rows, int Nq, int NqPad) {
+                  long long rows, int NqPad, SeqMap m, unsigned int* status) {
   constexpr int TPR = D / 8;                 // lanes per row
   constexpr int RPB = 256 / TPR;             // rows per block per sweep
   const int sub = threadIdx.x % TPR;
@@ -51,9 +52,14 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     const bool valid = row < rows;
     const long long bh = row / NqPad;
     const int r = static_cast<int>(row - bh * NqPad);
+    const int b = static_cast<int>(bh / m.Hq);
+    const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
+    const Seq sq = valid ? seq_of(m, b, status, 30) : Seq{0, 0, 0, 0, 0};
+    const bool live = valid && r < sq.nq;
+    const long long qrow = live ? row_q(m, sq, b, h, r) : 0;
     float acc = 0.f;
-    if (valid && r < Nq) {
-      const long long src = (bh * Nq + r) * TPR + sub;
+    if (live) {
+      const long long src = qrow * TPR + sub;
       float a[8], g[8];
       widen8<BF16>(__ldg(o + src), a);
       widen8<BF16>(__ldg(dO + src), g);
@@ -65,7 +71,7 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     if (!valid) continue;
     if (sub == 0) {
       Dv[row] = acc;
-      nLg[row] = (r < Nq) ? -lse[bh * Nq + r] * 1.4426950408889634f : __int_as_float(0xff800000);
+      nLg[row] = live ? -lse[qrow] * 1.4426950408889634f : __int_as_float(0xff800000);
     }
     if (dq_acc != nullptr) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -75,27 +81,32 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
   }
 }
 
-// Each thread converts 8 consecutive fp32 of one row to 16-bit.
+// Each thread converts 8 consecutive fp32 of one accumulator row to 16-bit;
+// accumulator rows are (b, h, padded q), and only rows of real queries are written.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
-dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, int Nq, int NqPad,
-                  float scale) {
+dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long long n8, int NqPad, float scale,
+                  SeqMap m, unsigned int* status) {
   constexpr int C8 = D / 8;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n8;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = idx / C8;            // row of dq: bh * Nq + r
+    const long long row = idx / C8;            // accumulator row: bh * NqPad + r
     const int c8 = static_cast<int>(idx - row * C8);
-    const long long bh = row / Nq;
-    const long long r = row - bh * Nq;
-    const long long src = ((bh * NqPad + r) * D) / 4 + 2 * c8;
+    const long long bh = row / NqPad;
+    const int r = static_cast<int>(row - bh * NqPad);
+    const int b = static_cast<int>(bh / m.Hq);
+    const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
+    const Seq sq = seq_of(m, b, status, 31);
+    if (r >= sq.nq) continue;
+    const long long src = (row * D) / 4 + 2 * c8;
     const float4 a = __ldcs(acc + src);
-    const float4 b = __ldcs(acc + src + 1);
+    const float4 c = __ldcs(acc + src + 1);
     uint4 out;
     out.x = pack2<BF16>(a.x * scale, a.y * scale);
     out.y = pack2<BF16>(a.z * scale, a.w * scale);
-    out.z = pack2<BF16>(b.x * scale, b.y * scale);
-    out.w = pack2<BF16>(b.z * scale, b.w * scale);
-    dq[idx] = out;
+    out.z = pack2<BF16>(c.x * scale, c.y * scale);
+    out.w = pack2<BF16>(c.z * scale, c.w * scale);
+    dq[row_q(m, sq, b, h, r) * C8 + c8] = out;
   }
 }
 
@@ -131,35 +142,41 @@ long long grid_for(long long work_items, int per_block) {
 
 template <int D, bool BF16>
 cudaError_t pre_t(const Problem& pb, const void* o, const void* dO, const float* lse, const Workspace& ws,
-                  cudaStream_t stream) {
+                  unsigned int* status, cudaStream_t stream) {
   const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.NqPad;
   const long long grid = grid_for(rows, 256 / (D / 8));
   preprocess_kernel<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
       static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws.nLg, ws.Dv,
-      pb.deterministic ? nullptr : reinterpret_cast<float4*>(ws.dq_acc), rows, pb.Nq, pb.NqPad);
+      pb.deterministic ? nullptr : reinterpret_cast<float4*>(ws.dq_acc), rows, pb.NqPad, seq_map(pb), status);
   return cudaGetLastError();
 }
 
 template <int D, bool BF16>
-cudaError_t conv_t(const Problem& pb, const Workspace& ws, void* dq, cudaStream_t stream) {
-  const long long n8 = static_cast<long long>(pb.B) * pb.Hq * pb.Nq * (D / 8);
+cudaError_t conv_t(const Problem& pb, const Workspace& ws, void* dq, unsigned int* status, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(pb.B) * pb.Hq * pb.NqPad * (D / 8);
   const long long grid = grid_for(n8, 256);
   dq_convert_kernel<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(ws.dq_acc), static_cast<uint4*>(dq), n8, pb.Nq, pb.NqPad, pb.scale);
+      reinterpret_cast<const float4*>(ws.dq_acc), static_cast<uint4*>(dq), n8, pb.NqPad, pb.scale, seq_map(pb),
+      status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, const float* lse,
-                              const Workspace& ws, cudaStream_t stream) {
-  if (pb.d == 128) return pb.bf16 ? pre_t<128, true>(pb, o, dO, lse, ws, stream) : pre_t<128, false>(pb, o, dO, lse, ws, stream);
-  return pb.bf16 ? pre_t<64, true>(pb, o, dO, lse, ws, stream) : pre_t<64, false>(pb, o, dO, lse, ws, stream);
+                              const Workspace& ws, unsigned int* status, cudaStream_t stream) {
+  if (pb.d == 128)
+    return pb.bf16 ? pre_t<128, true>(pb, o, dO, lse, ws, status, stream)
+                   : pre_t<128, false>(pb, o, dO, lse, ws, status, stream);
+  return pb.bf16 ? pre_t<64, true>(pb, o, dO, lse, ws, status, stream)
+                 : pre_t<64, false>(pb, o, dO, lse, ws, status, stream);
 }
 
-cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, cudaStream_t stream) {
-  if (pb.d == 128) return pb.bf16 ? conv_t<128, true>(pb, ws, dq, stream) : conv_t<128, false>(pb, ws, dq, stream);
-  return pb.bf16 ? conv_t<64, true>(pb, ws, dq, stream) : conv_t<64, false>(pb, ws, dq, stream);
+cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, unsigned int* status,
+                              cudaStream_t stream) {
+  if (pb.d == 128)
+    return pb.bf16 ? conv_t<128, true>(pb, ws, dq, status, stream) : conv_t<128, false>(pb, ws, dq, status, stream);
+  return pb.bf16 ? conv_t<64, true>(pb, ws, dq, status, stream) : conv_t<64, false>(pb, ws, dq, status, stream);
 }
 
 cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cudaStream_t stream) {

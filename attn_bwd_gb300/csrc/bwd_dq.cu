@@ -28,6 +28,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -69,9 +70,10 @@ struct Params {
   const float* Dv;
   void* dq;
   unsigned int* status;
-  int B, Hq, Hkv, Nq, Nkv, NqPad;
+  SeqMap m;
+  int B, Hq, Hkv, Nq, Nkv, NqPad;   // Nq, Nkv: the longest lengths of a packed batch
   float scale, scale_log2;
-  int causal, causal_off;
+  int causal;
 };
 
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -106,13 +108,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
-  const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const Seq sq = seq_of(p.m, b, p.status, 20);
+  const int zq = slab_q(p.m, b, h);                        // tensor-map slab of Q, dO
+  const int zk = slab_k(p.m, b, h / (p.Hq / p.Hkv));       // and of K, V
   const int q0 = i * BQ;
-  const int nKt = (p.Nkv + BK - 1) / BK;
-  const int qmax = min(q0 + BQ, p.Nq) - 1;
-  // causal: the last key any row of this tile sees is qmax + causal_off (none if negative)
-  const int kmax = qmax + p.causal_off;
-  const int T = p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
+  const int nKt = (sq.nk + BK - 1) / BK;
+  const int qmax = min(q0 + BQ, sq.nq) - 1;
+  // causal: the last key any row of this tile sees is qmax + delta (none if negative)
+  const int kmax = qmax + sq.delta;
+  const int T = q0 >= sq.nq ? 0 : p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
@@ -148,8 +152,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_arrive_expect_tx(bar(B_Q), 2 * L::TILE + 2 * BQ * 4);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
-        tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, q0, bh);
-        tma_load_3d(sb + L::OFF_DO + hh * L::HALF, &tm_do, bar(B_Q), 64 * hh, q0, bh);
+        tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, zq);
+        tma_load_3d(sb + L::OFF_DO + hh * L::HALF, &tm_do, bar(B_Q), 64 * hh, sq.q_start + q0, zq);
       }
       const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
       bulk_load(sb + L::OFF_LD, p.nLg + row, BQ * 4, bar(B_Q));
@@ -164,8 +168,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, t * BK, kvh);
-          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, t * BK, kvh);
+          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, zk);
+          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, zk);
         }
         issued = t + 1;
       }
@@ -246,8 +250,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int t = 0; ok && t < T; ++t) {
       const int kv0 = t * BK;
       // columns c >= lim are masked: past the end of K/V, or (causal) after query q
-      int lim = p.Nkv - kv0 - 64 * grp;
-      if (p.causal) lim = min(lim, q + p.causal_off - kv0 - 64 * grp + 1);
+      int lim = sq.nk - kv0 - 64 * grp;
+      if (p.causal) lim = min(lim, q + sq.delta - kv0 - 64 * grp + 1);
       const bool need_mask = __any_sync(0xffffffffu, lim < 64);
       const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK + 64 * grp;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 28))) break;
@@ -295,7 +299,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
-    uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + (static_cast<size_t>(bh) * p.Nq + q) * D * 2;
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + row_q(p.m, sq, b, h, q) * D * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 64; ++ch) {
       const int col = (D / 2) * grp + 32 * ch;
@@ -311,7 +315,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      if (q < p.Nq && !aborted) {
+      if (q < sq.nq && !aborted) {
         uint4* d4 = reinterpret_cast<uint4*>(out + col * 2);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
@@ -343,7 +347,7 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
   p.scale = a.pb.scale;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
-  p.causal_off = a.pb.causal_off;
+  p.m = seq_map(a.pb);
   const long long grid = static_cast<long long>((a.pb.Nq + BQ - 1) / BQ) * a.pb.B * a.pb.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();

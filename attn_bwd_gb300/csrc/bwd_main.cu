@@ -49,6 +49,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -106,9 +107,10 @@ struct Params {
   void* dk;
   void* dv;
   unsigned int* status;
-  int B, Hq, Hkv, Nq, Nkv, NqPad;
+  SeqMap m;
+  int B, Hq, Hkv, Nq, Nkv, NqPad;   // Nq, Nkv: the longest lengths of a packed batch
   float scale, scale_log2;
-  int causal, causal_off;
+  int causal;
 };
 
 // Bounded wait that ignores the abort flag: used only to drain work already
@@ -154,13 +156,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int b = gi / p.Hkv;
   const int hkv = gi - b * p.Hkv;
   const int G = p.Hq / p.Hkv;
+  const Seq sq = seq_of(p.m, b, p.status, 40);
   const int kv0 = j * BN;
-  const int nQt = (p.Nq + BM - 1) / BM;
-  // first query tile that sees this KV tile: causal, query q sees key kv0 when q >= kv0 - causal_off
-  const int qfirst = kv0 - p.causal_off;
+  const int nQt = (sq.nq + BM - 1) / BM;
+  // first query tile that sees this KV tile: causal, query q sees key kv0 when q >= kv0 - delta
+  const int qfirst = kv0 - sq.delta;
   const int i0 = p.causal ? (qfirst <= 0 ? 0 : min(qfirst / BM, nQt)) : 0;
   const int per_head = nQt - i0;
-  const int T = G * per_head;                          // tiles this CTA processes
+  const int T = kv0 < sq.nk ? G * per_head : 0;       // tiles this CTA processes
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV), 1);
@@ -197,12 +200,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0 && T > 0) {
-      const int kvh = b * p.Hkv + hkv;
+      const int kvh = slab_k(p.m, b, hkv);
       mbar_arrive_expect_tx(bar(B_KV), 2 * L::KV_BYTES);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
-        tma_load_3d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(B_KV), 64 * hh, kv0, kvh);
-        tma_load_3d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(B_KV), 64 * hh, kv0, kvh);
+        tma_load_3d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(B_KV), 64 * hh, sq.k_start + kv0, kvh);
+        tma_load_3d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(B_KV), 64 * hh, sq.k_start + kv0, kvh);
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -211,13 +214,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (t >= STAGES && !mbar_wait(bar(B_QEMPTY + s), ph ^ 1, wc, 1)) break;
         const int h = hkv * G + t / per_head;
         const int q0 = (i0 + t % per_head) * BM;
-        const int bh = b * p.Hq + h;
+        const int bh = b * p.Hq + h;                      // workspace rows are (b, h, padded q)
+        const int zq = slab_q(p.m, b, h);
         const uint32_t fb = bar(B_QFULL + s);
         mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + L::LD_BYTES);
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_3d(sb + L::OFF_Q + s * L::Q_BYTES + hh * L::QHALF, &tm_q, fb, 64 * hh, q0, bh);
-          tma_load_3d(sb + L::OFF_DO + s * L::Q_BYTES + hh * L::QHALF, &tm_do, fb, 64 * hh, q0, bh);
+          tma_load_3d(sb + L::OFF_Q + s * L::Q_BYTES + hh * L::QHALF, &tm_q, fb, 64 * hh, sq.q_start + q0, zq);
+          tma_load_3d(sb + L::OFF_DO + s * L::Q_BYTES + hh * L::QHALF, &tm_do, fb, 64 * hh, sq.q_start + q0, zq);
         }
         const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
         bulk_load(sb + L::OFF_LD + s * L::LD_BYTES, p.nLg + row, BM * 4, fb);
@@ -345,7 +349,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tdP = tmem + lane_off + L::COL_DP + 32 * grp;
     const int kv = kv0 + r;
-    const bool row_ok = kv < p.Nkv;
+    const bool row_ok = kv < sq.nk;
     uint8_t* ds_row = smem + L::OFF_DS + r * 128;
     const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
     int qi = i0;                                          // query tile of tile t (walked, no division)
@@ -358,7 +362,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // columns c < lim are masked: key kv lies after query q0 + 32 grp + c.
       // Only KV-tail rows and the diagonal tiles need the per-element test;
       // the decision is made once per warp.
-      const int lim = p.causal ? (kv - p.causal_off - q0 - 32 * grp) : INT_MIN;
+      const int lim = p.causal ? (kv - sq.delta - q0 - 32 * grp) : INT_MIN;
       const bool need_mask = __any_sync(0xffffffffu, !row_ok || lim > 0);
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 7))) break;
       tc_fence_after();
@@ -478,7 +482,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int kv = kv0 + r;
     const float mul = is_dk ? p.scale : 1.0f;
     uint8_t* out = reinterpret_cast<uint8_t*>(is_dk ? p.dk : p.dv) +
-                   (static_cast<size_t>(b * p.Hkv + hkv) * p.Nkv + kv) * D * 2;
+                   row_k(p.m, sq, b, hkv, kv) * D * 2;
     bool have = T > 0;
     if (have) {
       have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 13));
@@ -499,7 +503,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      if (kv < p.Nkv && !aborted) store_row_chunk<BF16>(out + ch * 64, pk);
+      if (kv < sq.nk && !aborted) store_row_chunk<BF16>(out + ch * 64, pk);
     }
   }
 
@@ -529,7 +533,7 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   p.scale = a.pb.scale;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
-  p.causal_off = a.pb.causal_off;
+  p.m = seq_map(a.pb);
   const long long nkt = (a.pb.Nkv + BN - 1) / BN;
   const long long grid = nkt * a.pb.B * a.pb.Hkv;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);

@@ -26,6 +26,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -64,9 +65,10 @@ struct Params {
   void* o;
   float* lse;
   unsigned int* status;
-  int B, Hq, Hkv, Nq, Nkv;
+  SeqMap m;
+  int B, Hq, Hkv, Nq, Nkv;   // Nq, Nkv: the longest lengths of a packed batch
   float scale_log2;
-  int causal, causal_off;
+  int causal;
 };
 
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -93,20 +95,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
-  // ---- work item: query tile i of head h of batch b; largest i first (longest under causal)
+  // ---- work item: query tile i of head h of sequence b; largest i first (longest under causal)
   const int BH = p.B * p.Hq;
   const int nQt = (p.Nq + BQ - 1) / BQ;
   const int i = nQt - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
-  const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const Seq sq = seq_of(p.m, b, p.status, 50);
+  const int zq = slab_q(p.m, b, h);                        // tensor-map slab of Q, O
+  const int zk = slab_k(p.m, b, h / (p.Hq / p.Hkv));       // and of K, V
   const int q0 = i * BQ;
-  const int nKt = (p.Nkv + BK - 1) / BK;
-  const int qmax = min(q0 + BQ, p.Nq) - 1;
-  // causal: the last key any row of this tile sees is qmax + causal_off (none if negative)
-  const int kmax = qmax + p.causal_off;
-  const int T = p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
+  const int nKt = (sq.nk + BK - 1) / BK;
+  const int qmax = min(q0 + BQ, sq.nq) - 1;
+  // causal: the last key any row of this tile sees is qmax + delta (none if negative)
+  const int kmax = qmax + sq.delta;
+  const int T = q0 >= sq.nq ? 0 : p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
@@ -139,7 +143,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (lane == 0 && T > 0) {
       mbar_arrive_expect_tx(bar(B_Q), L::TILE);
 #pragma unroll
-      for (int hh = 0; hh < L::NH; ++hh) tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, q0, bh);
+      for (int hh = 0; hh < L::NH; ++hh)
+        tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, zq);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % STAGES;
@@ -150,8 +155,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, t * BK, kvh);
-          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, t * BK, kvh);
+          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, zk);
+          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, zk);
         }
         issued = t + 1;
       }
@@ -217,8 +222,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     for (int t = 0; t < T; ++t) {
       const int kv0 = t * BK;
       // columns c >= lim are masked: past the end of K/V, or (causal) after query q
-      int lim = p.Nkv - kv0;
-      if (p.causal) lim = min(lim, q + p.causal_off - kv0 + 1);
+      int lim = sq.nk - kv0;
+      if (p.causal) lim = min(lim, q + sq.delta - kv0 + 1);
       const bool need_mask = __any_sync(0xffffffffu, lim < BK);
       const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 56))) { ok = false; break; }
@@ -292,7 +297,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     const bool aborted = *abort_flag != 0;
     const float inv = l > 0.f ? 1.f / l : 0.f;         // a row that saw no key: O = 0
-    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + q) * D * 2;
+    const long long orow = row_q(p.m, sq, b, h, q);
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + orow * D * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t pk[16];
@@ -307,14 +313,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      if (q < p.Nq && !aborted) {
+      if (q < sq.nq && !aborted) {
         uint4* d4 = reinterpret_cast<uint4*>(out + ch * 64);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
       }
     }
-    if (q < p.Nq && !aborted)
-      p.lse[static_cast<size_t>(bh) * p.Nq + q] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+    if (q < sq.nq && !aborted)
+      p.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
   }
 
   tc_fence_before();
@@ -339,7 +345,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
-  p.causal_off = a.pb.causal_off;
+  p.m = seq_map(a.pb);
   const long long grid = static_cast<long long>((a.pb.Nq + BQ - 1) / BQ) * a.pb.B * a.pb.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

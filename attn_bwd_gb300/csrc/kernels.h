@@ -21,15 +21,39 @@ struct Workspace {
   float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
 };
 
+// Geometry of the batch, passed to every kernel (see seq.cuh).
+struct SeqMap {
+  const int* cu_q;   // packed batch: [B + 1] query offsets (device); nullptr for a dense batch
+  const int* cu_k;   // packed batch: [B + 1] key offsets (device)
+  int B, Hq, Hkv;
+  int Nq, Nkv;       // dense: the lengths; packed: the longest lengths
+  int total_q, total_k;  // packed: rows per head
+  int causal_mode;   // 0 none, 1 top-left, 2 bottom-right
+};
+
 struct Problem {
-  int B, Hq, Hkv, Nq, Nkv, d;
+  int B, Hq, Hkv, Nq, Nkv, d;   // packed batch: Nq, Nkv are the longest lengths
   int NqPad;
   float scale;
-  int causal;
-  int causal_off;   // key j is masked for query i when causal and j > i + causal_off
+  int causal;        // any causal mask (causal_mode != 0)
+  int causal_mode;   // 0 none, 1 top-left, 2 bottom-right
   int bf16;
   int deterministic;
+  const int* cu_q;   // packed batch offsets, or nullptr
+  const int* cu_k;
+  int total_q, total_k;
 };
+
+inline SeqMap seq_map(const Problem& pb) {
+  SeqMap m;
+  m.cu_q = pb.cu_q;
+  m.cu_k = pb.cu_k;
+  m.B = pb.B; m.Hq = pb.Hq; m.Hkv = pb.Hkv;
+  m.Nq = pb.Nq; m.Nkv = pb.Nkv;
+  m.total_q = pb.total_q; m.total_k = pb.total_k;
+  m.causal_mode = pb.causal_mode;
+  return m;
+}
 
 struct MainArgs {
   Problem pb;
@@ -57,8 +81,9 @@ struct FwdArgs {
 
 // bwd_aux.cu
 cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, const float* lse,
-                              const Workspace& ws, cudaStream_t stream);
-cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, cudaStream_t stream);
+                              const Workspace& ws, unsigned int* status, cudaStream_t stream);
+cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, unsigned int* status,
+                              cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cudaStream_t stream);
 
 // bwd_main.cu: maps are Q, dO (box 64 x 64 rows), K, V (box 64 x 128 rows)

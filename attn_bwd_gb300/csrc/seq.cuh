@@ -1,0 +1,76 @@
+// seq.cuh -- where sequence b of a batch lives, for dense and packed batches.
+//
+// Dense batch:  Q-like tensors [B, Hq, Nq, d], K-like [B, Hkv, Nkv, d]; every
+//               sequence has Nq queries and Nkv keys.
+// Packed batch: Q-like tensors [Hq, total_q, d], K-like [Hkv, total_k, d];
+//               sequence b owns rows [cu_q[b], cu_q[b+1]) of every query head
+//               and [cu_k[b], cu_k[b+1]) of every key/value head, and attends
+//               only within itself.  Nq / Nkv then hold the longest lengths,
+//               which size the grids and the padded workspace rows.
+// The kernels address a head's rows as one "slab" of a 3-D view
+// (d, rows, slabs): slab b*H + h of Nq rows (dense) or slab h of total rows
+// starting at row cu[b] (packed).  Tensor maps use the same view.
+#pragma once
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace fa {
+
+struct Seq {
+  int nq, nk;            // queries and keys of this sequence
+  int q_start, k_start;  // first row of the sequence inside its slab
+  int delta;             // causal: key j masked for query i when j > i + delta
+};
+
+// Status code for a packed-batch offset array that is out of range.
+constexpr unsigned kStatusBadSeq = 10u;   // FA_ERR_ARG
+
+// Reads and checks the offsets of sequence b.  An offset pair outside
+// [0, total] or a length above the maximum is reported in the status word
+// and the sequence is treated as empty (nothing is read or written for it).
+__device__ __forceinline__ Seq seq_of(const SeqMap& m, int b, unsigned int* status, unsigned site) {
+  Seq s;
+  if (m.cu_q == nullptr) {
+    s.nq = m.Nq;
+    s.nk = m.Nkv;
+    s.q_start = 0;
+    s.k_start = 0;
+  } else {
+    const int q0 = __ldg(m.cu_q + b), q1 = __ldg(m.cu_q + b + 1);
+    const int k0 = __ldg(m.cu_k + b), k1 = __ldg(m.cu_k + b + 1);
+    const bool ok = q0 >= 0 && q0 <= q1 && q1 <= m.total_q && q1 - q0 <= m.Nq &&
+                    k0 >= 0 && k0 <= k1 && k1 <= m.total_k && k1 - k0 <= m.Nkv;
+    if (!ok) {
+      atomicCAS(status, 0u, (kStatusBadSeq << 16) | site);
+      s.nq = s.nk = s.q_start = s.k_start = 0;
+    } else {
+      s.nq = q1 - q0;
+      s.nk = k1 - k0;
+      s.q_start = q0;
+      s.k_start = k0;
+    }
+  }
+  s.delta = m.causal_mode == 2 ? s.nk - s.nq : 0;
+  return s;
+}
+
+// Slab index of query head h of sequence b in Q-like tensors, and of key/value
+// head hk in K-like tensors.
+__device__ __forceinline__ int slab_q(const SeqMap& m, int b, int h) { return m.cu_q ? h : b * m.Hq + h; }
+__device__ __forceinline__ int slab_k(const SeqMap& m, int b, int hk) { return m.cu_q ? hk : b * m.Hkv + hk; }
+
+// Rows per slab.
+__device__ __forceinline__ long long slab_rows_q(const SeqMap& m) { return m.cu_q ? m.total_q : m.Nq; }
+__device__ __forceinline__ long long slab_rows_k(const SeqMap& m) { return m.cu_q ? m.total_k : m.Nkv; }
+
+// Row index (into [slabs * rows]) of query r of head h of sequence s (b), and of key r.
+__device__ __forceinline__ long long row_q(const SeqMap& m, const Seq& s, int b, int h, int r) {
+  return static_cast<long long>(slab_q(m, b, h)) * slab_rows_q(m) + s.q_start + r;
+}
+__device__ __forceinline__ long long row_k(const SeqMap& m, const Seq& s, int b, int hk, int r) {
+  return static_cast<long long>(slab_k(m, b, hk)) * slab_rows_k(m) + s.k_start + r;
+}
+
+}  // namespace fa

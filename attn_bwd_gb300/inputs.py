@@ -110,3 +110,59 @@ def llama_gqa(n: int) -> Shape:
 
 LLAMA_SWEEP = [2 ** p for p in range(5, 15)]
 HEADLINE = llama_gqa(8192)
+
+
+@dataclasses.dataclass(frozen=True)
+class Packed:
+    """A packed batch of sequences of different lengths: Q/O/dO are [Hq, total_q, d],
+    K/V are [Hkv, total_k, d]; sequence b owns rows cu_q[b]..cu_q[b+1] (and cu_k) of every head."""
+
+    lens_q: tuple
+    lens_k: tuple
+    Hq: int
+    Hkv: int
+    d: int
+    causal: int
+    dtype: str = "bf16"
+
+    @property
+    def cu_q(self):
+        return [0] + [int(x) for x in torch.tensor(self.lens_q).cumsum(0).tolist()]
+
+    @property
+    def cu_k(self):
+        return [0] + [int(x) for x in torch.tensor(self.lens_k).cumsum(0).tolist()]
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def name(self) -> str:
+        c = {0: "full", 1: "causal", 2: "causalbr"}[int(self.causal)]
+        return (f"q{'-'.join(map(str, self.lens_q))}_k{'-'.join(map(str, self.lens_k))}"
+                f"_Hq{self.Hq}_Hkv{self.Hkv}_d{self.d}_{self.dtype}_{c}")
+
+
+def draw_packed(pk: Packed, seed: int, device: str | torch.device = "cpu"):
+    """(q, k, v, do) of a packed batch, N(0,1) drawn in fp32 from one seeded generator, rounded once."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    tq, tk = sum(pk.lens_q), sum(pk.lens_k)
+    sizes = [(pk.Hq, tq, pk.d), (pk.Hkv, tk, pk.d), (pk.Hkv, tk, pk.d), (pk.Hq, tq, pk.d)]
+    return tuple(torch.randn(sz, generator=gen, device=device, dtype=torch.float32).to(pk.torch_dtype)
+                 for sz in sizes)
+
+
+def packed_mix():
+    """Length mixes for packed-batch parity: single rows, empty sequences, ragged tails past
+    one and two tiles, Nq < Nkv and Nq > Nkv within one batch, both head dims."""
+    out = []
+    for c in (0, 1, 2):
+        out.append(Packed((1, 130, 0, 257, 64), (1, 130, 5, 257, 64), 4, 2, 128, c, "bf16"))
+        out.append(Packed((77, 300, 16), (200, 130, 16), 2, 1, 64, c, "f16"))
+    out.append(Packed((50, 20, 129), (0, 33, 129), 2, 2, 128, 0, "bf16"))   # a sequence with no keys
+    return out

@@ -73,3 +73,59 @@ def backward(q, k, v, o, do, lse, scale: float, causal, deterministic: bool = Fa
     _check(_lib.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, _DT[q.dtype],
                        int(deterministic), ws, ws.numel(), s), "fa_bwd")
     return dq, dk, dv
+
+
+# ------------------------------------------------------------ packed batches
+
+def _cu(cu, device):
+    """Offsets as a device int32 tensor, plus the lengths as host ints."""
+    if isinstance(cu, torch.Tensor):
+        host = [int(x) for x in cu.detach().cpu().tolist()]
+    else:
+        host = [int(x) for x in cu]
+    dev = torch.tensor(host, dtype=torch.int32, device=device)
+    lens = [b - a for a, b in zip(host, host[1:])]
+    return dev, host, lens
+
+
+def forward_varlen(q, k, v, cu_q, cu_k, scale: float, causal, max_q=None, max_k=None, stream=None):
+    """Packed batch: q [Hq, total_q, d], k/v [Hkv, total_k, d]; cu_* are B + 1 offsets.
+    Returns (O like q, L fp32 [Hq, total_q])."""
+    _need(q, k, v)
+    Hq, total_q, d = q.shape
+    Hkv, total_k, _ = k.shape
+    dq_, hq, lq = _cu(cu_q, q.device)
+    dk_, hk, lk = _cu(cu_k, q.device)
+    B = len(lq)
+    max_q = max_q if max_q is not None else max(max(lq), 1)
+    max_k = max_k if max_k is not None else max(max(lk), 1)
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, total_q, dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_fwd_varlen(q, k, v, o, lse, dq_, dk_, B, Hq, Hkv, total_q, total_k, max_q, max_k, d, scale,
+                              causal, _DT[q.dtype], s), "fa_fwd_varlen")
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale: float, causal, deterministic: bool = False,
+                    max_q=None, max_k=None, out=None, stream=None):
+    """Packed-batch backward.  Returns (dQ, dK, dV) in the packed layouts."""
+    _need(q, k, v, o, do, lse)
+    Hq, total_q, d = q.shape
+    Hkv, total_k, _ = k.shape
+    dq_, hq, lq = _cu(cu_q, q.device)
+    dk_, hk, lk = _cu(cu_k, q.device)
+    B = len(lq)
+    max_q = max_q if max_q is not None else max(max(lq), 1)
+    max_k = max_k if max_k is not None else max(max(lk), 1)
+    n = _lib.fa_bwd_varlen_workspace_size(B, Hq, Hkv, max_q, max_k, d, int(deterministic))
+    if n == 0:
+        raise ValueError("invalid shape for the backward")
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, dq_, dk_, B, Hq, Hkv, total_q, total_k, max_q, max_k,
+                              d, scale, causal, _DT[q.dtype], int(deterministic), ws, n, s), "fa_bwd_varlen")
+    return dq, dk, dv

@@ -185,14 +185,52 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
                    int dtype, int deterministic, cudaStream_t stream);
 
+/*
+ * Packed variable-length batches.  "[Kernel] Flash attention 2" (Liger-Kernel
+ * #275, "Details") supports different Q and KV lengths with no restriction on
+ * the sequence length; these entry points take a batch of sequences of
+ * different lengths packed along the row axis of every head:
+ *   Q, O, dO, dQ : [Hq,  total_q, d]   16-bit
+ *   K, V, dK, dV : [Hkv, total_k, d]   16-bit
+ *   L (lse)      : [Hq,  total_q]      fp32
+ * Sequence b owns rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of every query
+ * head and rows [cu_seqlens_k[b], cu_seqlens_k[b+1]) of every key/value head,
+ * and attends only to its own keys; causal alignment (fa_causal) is taken per
+ * sequence.  A sequence may be empty; one with queries but no keys gets O = 0,
+ * L = -inf, dQ = 0.  Rows not covered by any sequence are left untouched.
+ * cu_seqlens_q / cu_seqlens_k: DEVICE int32 arrays of B + 1 offsets (4-byte
+ * aligned), starting at 0, non-decreasing, ending at total_q / total_k, each
+ * length at most max_q / max_k.  The host cannot read them without a
+ * synchronisation, so the kernels check every sequence's offsets before using
+ * them: a sequence whose offsets leave [0, total] or exceed the maximum is
+ * skipped (nothing of it is read or written) and fa_last_device_error()
+ * reports FA_ERR_ARG.  total_q, total_k: 1 .. 2^30; max_q, max_k: 1 .. FA_MAX_SEQ.
+ * Workspace: fa_bwd_varlen_workspace_size(), rows padded per (sequence, query
+ * head) to a multiple of 128 of max_q.  Other arguments as for fa_fwd / fa_bwd.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  int B, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k,
+                  int d, float scale, int causal, int dtype, cudaStream_t stream);
+
+size_t fa_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int max_q, int max_k, int d, int deterministic);
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                  const float* lse, void* dq, void* dk, void* dv,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  int B, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k,
+                  int d, float scale, int causal, int dtype, int deterministic,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of an fa_status value (static string, never NULL). */
 const char* fa_strerror(int status);
 
 /*
  * fa_last_device_error -- synchronises `stream`, then reads and clears the
  * device status words.  Returns FA_ERR_DEVICE_TIMEOUT if any bounded wait in
- * a kernel ran out since the last call, FA_ERR_CUDA if the sync failed,
- * FA_OK otherwise.
+ * a kernel ran out since the last call, FA_ERR_ARG if a kernel skipped a
+ * packed-batch sequence with out-of-range offsets, FA_ERR_CUDA if the sync
+ * failed, FA_OK otherwise.
  */
 int fa_last_device_error(cudaStream_t stream);
 

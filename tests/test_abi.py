@@ -111,3 +111,51 @@ def test_stage_entry_points_validate(lib):
     assert _lib.fa_bwd_dq(A, A, A, A, None, 1, 2, 1, 8, 8, 64, 0.1, 0, 0, 1, W, 1 << 30) == _lib.FA_ERR_NULL
     assert _lib.fa_selftest_wait_timeout(0) == _lib.FA_ERR_ARG
     assert _lib.fa_selftest_wait_timeout(10_000_000) == _lib.FA_ERR_ARG
+
+
+C = 0x300000       # fake, 4-byte-aligned device offset arrays
+
+
+def _bwd_varlen(**kw):
+    args = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, dq=A, dk=A, dv=A, cu_q=C, cu_k=C + 64, B=2, Hq=2, Hkv=1,
+                total_q=100, total_k=80, max_q=60, max_k=50, d=64, scale=0.125, causal=0, dtype=_lib.FA_BF16,
+                deterministic=0, workspace=W, workspace_bytes=0)
+    args.update(kw)
+    return _lib.fa_bwd_varlen(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_q=None), _lib.FA_ERR_NULL),
+    (dict(cu_k=None), _lib.FA_ERR_NULL),
+    (dict(dq=None), _lib.FA_ERR_NULL),
+    (dict(cu_q=C + 2), _lib.FA_ERR_ALIGN),
+    (dict(cu_k=C + 1), _lib.FA_ERR_ALIGN),
+    (dict(q=A + 8), _lib.FA_ERR_ALIGN),
+    (dict(total_q=0), _lib.FA_ERR_SHAPE),
+    (dict(total_k=(1 << 30) + 1), _lib.FA_ERR_SHAPE),
+    (dict(max_q=0), _lib.FA_ERR_SHAPE),
+    (dict(max_k=(1 << 24) + 1), _lib.FA_ERR_SHAPE),
+    (dict(B=0), _lib.FA_ERR_SHAPE),
+    (dict(d=80), _lib.FA_ERR_HEADDIM),
+    (dict(Hq=3, Hkv=2), _lib.FA_ERR_GQA),
+    (dict(causal=5), _lib.FA_ERR_ARG),
+    (dict(workspace_bytes=100), _lib.FA_ERR_WORKSPACE),
+])
+def test_bwd_varlen_rejects_bad_arguments(lib, kw, code):
+    assert _bwd_varlen(**kw) == code
+
+
+def test_fwd_varlen_rejects_bad_arguments(lib):
+    f = _lib.fa_fwd_varlen
+    ok = dict(q=A, k=A, v=A, o=A, lse=A, cu_q=C, cu_k=C, B=1, Hq=2, Hkv=1, total_q=10, total_k=10, max_q=10,
+              max_k=10, d=64, scale=0.1, causal=1, dtype=0)
+    assert f(**{**ok, "cu_k": None}) == _lib.FA_ERR_NULL
+    assert f(**{**ok, "lse": A + 4}) == _lib.FA_ERR_ALIGN
+    assert f(**{**ok, "total_q": -1}) == _lib.FA_ERR_SHAPE
+    assert f(**{**ok, "scale": float("nan")}) == _lib.FA_ERR_ARG
+
+
+def test_varlen_workspace_matches_dense_at_the_longest_length(lib):
+    for det in (0, 1):
+        assert (_lib.fa_bwd_varlen_workspace_size(3, 4, 2, 300, 200, 128, det)
+                == _lib.fa_bwd_workspace_size(3, 4, 2, 300, 200, 128, det))
