@@ -73,7 +73,7 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 int check_shape(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int dtype) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1) return FA_ERR_SHAPE;
   if (Nq > FA_MAX_SEQ || Nkv > FA_MAX_SEQ || B > 65535 || Hq > 65535) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (d < 8 || d > 128 || d % 8 != 0) return FA_ERR_HEADDIM;   // served by the d = 64 / 128 kernels
   if (Hq % Hkv != 0) return FA_ERR_GQA;
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   // grid-size limits of the largest launch (one CTA per 64 query rows x head x batch)
@@ -86,10 +86,13 @@ int check_shape(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int dtype) {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// The fp32 dQ accumulator rows are as wide as the kernel that fills them (64 or 128).
+int kernel_d(int d) { return d <= 64 ? 64 : 128; }
+
 size_t ws_bytes(int B, int Hq, int Nq, int d, int deterministic) {
   const size_t rows = static_cast<size_t>(B) * Hq * round_up(Nq, kRowPad);
   size_t total = 2 * align_up(rows * sizeof(float));
-  if (!deterministic) total += align_up(rows * d * sizeof(float));
+  if (!deterministic) total += align_up(rows * kernel_d(d) * sizeof(float));
   return total;
 }
 
@@ -294,7 +297,7 @@ const char* fa_strerror(int status) {
     case FA_OK: return "ok";
     case FA_ERR_NULL: return "a required pointer is NULL";
     case FA_ERR_SHAPE: return "invalid shape (a size < 1 or above the supported limit)";
-    case FA_ERR_HEADDIM: return "head dimension must be 64 or 128";
+    case FA_ERR_HEADDIM: return "head dimension must be a multiple of 8 from 8 to 128";
     case FA_ERR_GQA: return "Hq must be a multiple of Hkv";
     case FA_ERR_ALIGN: return "a pointer is not 16-byte aligned (workspace: 256-byte)";
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_size()";

@@ -58,8 +58,8 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     const bool live = valid && r < sq.nq;
     const long long qrow = live ? row_q(m, sq, b, h, r) : 0;
     float acc = 0.f;
-    if (live) {
-      const long long src = qrow * TPR + sub;
+    if (live && 8 * sub < m.d) {
+      const long long src = qrow * (m.d / 8) + sub;
       float a[8], g[8];
       widen8<BF16>(__ldg(o + src), a);
       widen8<BF16>(__ldg(dO + src), g);
@@ -97,7 +97,7 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
     const int b = static_cast<int>(bh / m.Hq);
     const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
     const Seq sq = seq_of(m, b, status, 31);
-    if (r >= sq.nq) continue;
+    if (r >= sq.nq || 8 * c8 >= m.d) continue;
     const long long src = (row * D) / 4 + 2 * c8;
     const float4 a = __ldcs(acc + src);
     const float4 c = __ldcs(acc + src + 1);
@@ -106,7 +106,7 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
     out.y = pack2<BF16>(a.z * scale, a.w * scale);
     out.z = pack2<BF16>(c.x * scale, c.y * scale);
     out.w = pack2<BF16>(c.z * scale, c.w * scale);
-    dq[row_q(m, sq, b, h, r) * C8 + c8] = out;
+    dq[row_q(m, sq, b, h, r) * (m.d / 8) + c8] = out;
   }
 }
 
@@ -165,7 +165,7 @@ cudaError_t conv_t(const Problem& pb, const Workspace& ws, void* dq, unsigned in
 
 cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, const float* lse,
                               const Workspace& ws, unsigned int* status, cudaStream_t stream) {
-  if (pb.d == 128)
+  if (pb.d > 64)
     return pb.bf16 ? pre_t<128, true>(pb, o, dO, lse, ws, status, stream)
                    : pre_t<128, false>(pb, o, dO, lse, ws, status, stream);
   return pb.bf16 ? pre_t<64, true>(pb, o, dO, lse, ws, status, stream)
@@ -174,7 +174,7 @@ cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, 
 
 cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, unsigned int* status,
                               cudaStream_t stream) {
-  if (pb.d == 128)
+  if (pb.d > 64)
     return pb.bf16 ? conv_t<128, true>(pb, ws, dq, status, stream) : conv_t<128, false>(pb, ws, dq, status, stream);
   return pb.bf16 ? conv_t<64, true>(pb, ws, dq, status, stream) : conv_t<64, false>(pb, ws, dq, status, stream);
 }

@@ -299,7 +299,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
-    uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + row_q(p.m, sq, b, h, q) * D * 2;
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + row_q(p.m, sq, b, h, q) * p.m.d * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 64; ++ch) {
       const int col = (D / 2) * grp + 32 * ch;
@@ -318,7 +318,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (q < sq.nq && !aborted) {
         uint4* d4 = reinterpret_cast<uint4*>(out + col * 2);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+        for (int k4 = 0; k4 < 4; ++k4)
+          if (col + 8 * k4 < p.m.d) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
       }
     }
   }
@@ -357,7 +358,7 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
 
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  if (a.pb.d == 128)
+  if (a.pb.d > 64)
     return a.pb.bf16 ? launch_t<128, true>(a, tq, tdo, tk, tv, stream) : launch_t<128, false>(a, tq, tdo, tk, tv, stream);
   return a.pb.bf16 ? launch_t<64, true>(a, tq, tdo, tk, tv, stream) : launch_t<64, false>(a, tq, tdo, tk, tv, stream);
 }

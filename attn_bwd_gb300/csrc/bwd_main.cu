@@ -122,11 +122,13 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Stores the 16-byte pieces of a 32-column chunk that lie within the row's `cols` columns.
 template <bool BF16>
-__device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&pk)[16]) {
+__device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&pk)[16], int cols) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  for (int i = 0; i < 4; ++i)
+    if (8 * i < cols) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
 template <int D, bool BF16, bool DET>
@@ -482,7 +484,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int kv = kv0 + r;
     const float mul = is_dk ? p.scale : 1.0f;
     uint8_t* out = reinterpret_cast<uint8_t*>(is_dk ? p.dk : p.dv) +
-                   row_k(p.m, sq, b, hkv, kv) * D * 2;
+                   row_k(p.m, sq, b, hkv, kv) * p.m.d * 2;
     bool have = T > 0;
     if (have) {
       have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 13));
@@ -503,7 +505,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      if (kv < sq.nk && !aborted) store_row_chunk<BF16>(out + ch * 64, pk);
+      if (kv < sq.nk && !aborted) store_row_chunk<BF16>(out + ch * 64, pk, p.m.d - 32 * ch);
     }
   }
 
@@ -545,7 +547,7 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   const bool det = a.pb.deterministic != 0;
-  if (a.pb.d == 128) {
+  if (a.pb.d > 64) {
     if (a.pb.bf16) return det ? launch_t<128, true, true>(a, tq, tdo, tk, tv, stream)
                               : launch_t<128, true, false>(a, tq, tdo, tk, tv, stream);
     return det ? launch_t<128, false, true>(a, tq, tdo, tk, tv, stream)

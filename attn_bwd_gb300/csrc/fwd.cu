@@ -298,7 +298,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const bool aborted = *abort_flag != 0;
     const float inv = l > 0.f ? 1.f / l : 0.f;         // a row that saw no key: O = 0
     const long long orow = row_q(p.m, sq, b, h, q);
-    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + orow * D * 2;
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + orow * p.m.d * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t pk[16];
@@ -316,7 +316,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (q < sq.nq && !aborted) {
         uint4* d4 = reinterpret_cast<uint4*>(out + ch * 64);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+        for (int k4 = 0; k4 < 4; ++k4)
+          if (32 * ch + 8 * k4 < p.m.d) d4[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
       }
     }
     if (q < sq.nq && !aborted)
@@ -355,7 +356,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        unsigned int* status, cudaStream_t stream) {
-  if (a.pb.d == 128)
+  if (a.pb.d > 64)
     return a.pb.bf16 ? launch_t<128, true>(a, tq, tk, tv, status, stream)
                      : launch_t<128, false>(a, tq, tk, tv, status, stream);
   return a.pb.bf16 ? launch_t<64, true>(a, tq, tk, tv, status, stream)

@@ -26,6 +26,7 @@ struct SeqMap {
   const int* cu_q;   // packed batch: [B + 1] query offsets (device); nullptr for a dense batch
   const int* cu_k;   // packed batch: [B + 1] key offsets (device)
   int B, Hq, Hkv;
+  int d;             // head dimension of the tensors (<= the kernel's D; missing columns read as 0)
   int Nq, Nkv;       // dense: the lengths; packed: the longest lengths
   int total_q, total_k;  // packed: rows per head
   int causal_mode;   // 0 none, 1 top-left, 2 bottom-right
@@ -49,6 +50,7 @@ inline SeqMap seq_map(const Problem& pb) {
   m.cu_q = pb.cu_q;
   m.cu_k = pb.cu_k;
   m.B = pb.B; m.Hq = pb.Hq; m.Hkv = pb.Hkv;
+  m.d = pb.d;
   m.Nq = pb.Nq; m.Nkv = pb.Nkv;
   m.total_q = pb.total_q; m.total_k = pb.total_k;
   m.causal_mode = pb.causal_mode;

@@ -165,4 +165,5 @@ def packed_mix():
         out.append(Packed((1, 130, 0, 257, 64), (1, 130, 5, 257, 64), 4, 2, 128, c, "bf16"))
         out.append(Packed((77, 300, 16), (200, 130, 16), 2, 1, 64, c, "f16"))
     out.append(Packed((50, 20, 129), (0, 33, 129), 2, 2, 128, 0, "bf16"))   # a sequence with no keys
+    out.append(Packed((33, 190, 1), (65, 140, 7), 4, 1, 80, 2, "bf16"))     # head dim 80
     return out

@@ -27,7 +27,14 @@
  *   Q, O, dO, dQ : [B, Hq,  Nq,  d]   16-bit (fp16 or bf16, see fa_dtype)
  *   K, V, dK, dV : [B, Hkv, Nkv, d]   16-bit
  *   L (lse)      : [B, Hq,  Nq]       fp32, natural-log LSE of the scaled scores
- * d must be 64 or 128.  Every pointer is a DEVICE pointer on the current
+ * d: a multiple of 8 from 8 to 128 ("[Kernel] Flash attention 2", "Details":
+ * no restriction on the head dimension; 8 keeps every row a whole number of
+ * 16-byte pieces, and 128 is the most whose dK and dV accumulators, 128 rows x
+ * d fp32 each, leave room in the 512 TMEM columns for the score, dP and dQ
+ * tiles).  Other sizes run on the d = 64 or d = 128 kernels, which read the
+ * missing columns as zeros: exact, since a zero column adds nothing to Q K^T
+ * and produces a zero column of O, dQ, dK, dV, which is not written.
+ * Every pointer is a DEVICE pointer on the current
  * device, 16-byte aligned.  The caller owns every buffer (inputs, outputs and
  * workspace) and the stream; the library allocates no device memory, keeps no
  * state besides one status word per kernel family, and never synchronises
@@ -52,7 +59,7 @@ typedef enum {
   FA_OK = 0,
   FA_ERR_NULL = 1,            /* a required pointer is NULL                         */
   FA_ERR_SHAPE = 2,           /* B, Hq, Hkv, Nq or Nkv < 1, or above the size limit */
-  FA_ERR_HEADDIM = 3,         /* d not in {64, 128}                                 */
+  FA_ERR_HEADDIM = 3,         /* d not a multiple of 8 in [8, 128]                  */
   FA_ERR_GQA = 4,             /* Hq not a multiple of Hkv                           */
   FA_ERR_ALIGN = 5,           /* a pointer is not 16-byte aligned                   */
   FA_ERR_WORKSPACE = 6,       /* workspace NULL or smaller than fa_bwd_workspace_size */
@@ -173,7 +180,7 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void*
  * Limit: returns FA_ERR_WORKSPACE, launching nothing, when
  * fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, deterministic) exceeds
  * FA_STATIC_SCRATCH_BYTES (deterministic mode needs 8 bytes per query row,
- * rows padded to 128 per head; atomic mode 8 + 4*d bytes per padded row).
+ * rows padded to 128 per head; atomic mode 8 + 4*64 (d <= 64) or 8 + 4*128 bytes per padded row).
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture.  All calls share the one array, and each call rewrites

@@ -52,7 +52,10 @@ def test_workspace_size_formula(lib):
     assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 0) == 2 * rows * 4 + rows * 64 * 4
     assert _lib.fa_bwd_workspace_size(2, 4, 3, 100, 100, 64, 0) == 0     # GQA mismatch
     assert _lib.fa_bwd_workspace_size(2, 4, 4, 0, 100, 64, 0) == 0       # empty sequence
-    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 96, 0) == 0     # head dim
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 100, 0) == 0    # head dim
+    # other head dims use the accumulator width of the kernel that serves them (64 or 128)
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 96, 0) == 2 * rows * 4 + rows * 128 * 4
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 40, 0) == 2 * rows * 4 + rows * 64 * 4
 
 
 def _bwd(**kw):
@@ -70,7 +73,9 @@ def _bwd(**kw):
     (dict(Nkv=-3), _lib.FA_ERR_SHAPE),
     (dict(B=0), _lib.FA_ERR_SHAPE),
     (dict(Nq=(1 << 24) + 1), _lib.FA_ERR_SHAPE),
-    (dict(d=96), _lib.FA_ERR_HEADDIM),
+    (dict(d=100), _lib.FA_ERR_HEADDIM),
+    (dict(d=4), _lib.FA_ERR_HEADDIM),
+    (dict(d=136), _lib.FA_ERR_HEADDIM),
     (dict(d=256), _lib.FA_ERR_HEADDIM),
     (dict(Hq=3, Hkv=2), _lib.FA_ERR_GQA),
     (dict(dtype=7), _lib.FA_ERR_DTYPE),
@@ -99,7 +104,7 @@ def test_deterministic_workspace_is_smaller(lib):
 def test_fwd_rejects_bad_arguments(lib):
     f = _lib.fa_fwd
     assert f(None, A, A, A, A, 1, 2, 1, 8, 8, 64, 0.1, 0, 0) == _lib.FA_ERR_NULL
-    assert f(A, A, A, A, A, 1, 2, 1, 8, 8, 32, 0.1, 0, 0) == _lib.FA_ERR_HEADDIM
+    assert f(A, A, A, A, A, 1, 2, 1, 8, 8, 33, 0.1, 0, 0) == _lib.FA_ERR_HEADDIM
     assert f(A, A, A, A, A, 1, 3, 2, 8, 8, 64, 0.1, 0, 0) == _lib.FA_ERR_GQA
     assert f(A, A, A, A, A + 4, 1, 2, 1, 8, 8, 64, 0.1, 0, 0) == _lib.FA_ERR_ALIGN
     assert f(A, A, A, A, A, 1, 2, 1, 8, 8, 64, 0.1, 0, 2) == _lib.FA_ERR_DTYPE
@@ -136,7 +141,7 @@ def _bwd_varlen(**kw):
     (dict(max_q=0), _lib.FA_ERR_SHAPE),
     (dict(max_k=(1 << 24) + 1), _lib.FA_ERR_SHAPE),
     (dict(B=0), _lib.FA_ERR_SHAPE),
-    (dict(d=80), _lib.FA_ERR_HEADDIM),
+    (dict(d=84), _lib.FA_ERR_HEADDIM),
     (dict(Hq=3, Hkv=2), _lib.FA_ERR_GQA),
     (dict(causal=5), _lib.FA_ERR_ARG),
     (dict(workspace_bytes=100), _lib.FA_ERR_WORKSPACE),

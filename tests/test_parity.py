@@ -215,6 +215,20 @@ def test_bottom_right_causal(shape, det):
     check_full(shape, 11, det)
 
 
+@pytest.mark.parametrize("det", [False, True])
+@pytest.mark.parametrize("shape", [
+    inputs.Shape(1, 2, 1, 70, 90, 8, 1, "bf16"),
+    inputs.Shape(2, 4, 2, 130, 130, 32, 0, "f16"),
+    inputs.Shape(1, 4, 4, 200, 150, 40, 2, "bf16"),
+    inputs.Shape(1, 6, 2, 129, 257, 72, 1, "bf16"),
+    inputs.Shape(2, 2, 1, 256, 256, 96, 1, "f16"),
+    inputs.Shape(1, 2, 2, 100, 300, 120, 0, "bf16"),
+], ids=lambda s: s.name())
+def test_other_head_dims(shape, det):
+    """Head dims other than 64 / 128 run on those kernels with the missing columns read as zero."""
+    check_full(shape, 12, det)
+
+
 def test_outputs_are_overwritten_not_accumulated():
     shape = inputs.Shape(1, 2, 1, 150, 150, 64, True, "f16")
     q, k, v, do = (t.cuda() for t in inputs.draw(shape, 10))
