@@ -32,6 +32,14 @@ FA_CAUSAL_NONE = 0
 FA_CAUSAL_TOP_LEFT = 1
 FA_CAUSAL_BOTTOM_RIGHT = 2
 
+class fa_stride3(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_longlong), ("h", ctypes.c_longlong), ("n", ctypes.c_longlong)]
+
+
+class fa_strides(ctypes.Structure):
+    _fields_ = [(n, fa_stride3) for n in ("q", "k", "v", "o", "dO", "dq", "dk", "dv", "lse")]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
@@ -52,6 +60,10 @@ _SIGNATURES = {
     "fa_bwd_varlen_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                            _I, _P, _S, _P]),
+    "fa_fwd_strided": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(fa_strides), _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                            _F, _I, _I, _P]),
+    "fa_bwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(fa_strides), _P, _P, _I, _I, _I, _I,
+                            _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
 }
 
 FA_STATIC_SCRATCH_BYTES = 64 << 20
@@ -167,3 +179,28 @@ def fa_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_q, cu_k, B, Hq, Hkv, total
                                 _ptr(dv), _ptr(cu_q), _ptr(cu_k), B, Hq, Hkv, total_q, total_k, max_q, max_k, d,
                                 float(scale), int(causal), int(dtype), int(deterministic), _ptr(workspace),
                                 int(workspace_bytes), _stream(stream))
+
+
+def make_strides(**kw) -> fa_strides:
+    """fa_strides from (b, h, n) element-stride triples keyed q, k, v, o, dO, dq, dk, dv, lse."""
+    st = fa_strides()
+    for name, (b, h, n) in kw.items():
+        setattr(st, name, fa_stride3(int(b), int(h), int(n)))
+    return st
+
+
+def fa_fwd_strided(q, k, v, o, lse, strides, cu_q, cu_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k, d, scale, causal,
+                   dtype, stream=None) -> int:
+    sp = ctypes.byref(strides) if strides is not None else None
+    return load().fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), sp, _ptr(cu_q), _ptr(cu_k), B, Hq,
+                                 Hkv, Nq, Nkv, total_q, total_k, d, float(scale), int(causal), int(dtype),
+                                 _stream(stream))
+
+
+def fa_bwd_strided(q, k, v, o, dO, lse, dq, dk, dv, strides, cu_q, cu_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k, d,
+                   scale, causal, dtype, deterministic, workspace, workspace_bytes, stream=None) -> int:
+    sp = ctypes.byref(strides) if strides is not None else None
+    return load().fa_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), sp, _ptr(cu_q), _ptr(cu_k), B, Hq, Hkv, Nq, Nkv, total_q, total_k, d,
+                                 float(scale), int(causal), int(dtype), int(deterministic), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))

@@ -53,15 +53,19 @@ int get_encoder() {
   return FA_OK;
 }
 
-// 3-D view [heads][rows][d] of a contiguous 16-bit tensor; box = 64 columns x box_rows rows,
-// 128-byte swizzle (one box row is exactly 128 bytes).  Rows past `rows` read as zero.
-int make_map(CUtensorMap* m, const void* base, int bf16, int d, int rows, long long heads, int box_rows) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
-                              static_cast<cuuint64_t>(heads)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+// 4-D view (d, rows, heads, batch) of a 16-bit tensor with element strides s
+// for the row, head and batch axes; box = 64 columns x box_rows rows of one
+// head, 128-byte swizzle (one box row is exactly 128 bytes).  Columns past d
+// and rows past `rows` read as zero.
+int make_map(CUtensorMap* m, const void* base, int bf16, int d, int rows, int heads, int batch, Str3 s,
+             int box_rows) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n) * 2, static_cast<cuuint64_t>(s.h) * 2,
+                                 static_cast<cuuint64_t>(s.b) * 2};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_rows), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -115,17 +119,41 @@ struct Geo {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
-  long long slabs_q() const { return cu_q ? Hq : static_cast<long long>(B) * Hq; }
-  long long slabs_k() const { return cu_q ? Hkv : static_cast<long long>(B) * Hkv; }
+  Strides st;        // element strides of every tensor
+  int batch() const { return cu_q ? 1 : B; }
   int rows_q() const { return cu_q ? total_q : Nq; }
   int rows_k() const { return cu_q ? total_k : Nkv; }
 };
 
-Geo dense(int B, int Hq, int Hkv, int Nq, int Nkv, int d) { return Geo{B, Hq, Hkv, Nq, Nkv, d, nullptr, nullptr, Nq, Nkv}; }
+// Strides of contiguous [batch, heads, rows, d] tensors (and [batch, heads, rows] for L).
+Str3 contiguous(int heads, long long rows, int d) {
+  return Str3{heads * rows * d, rows * d, d};
+}
+
+Strides contiguous_all(int Hq, int Hkv, long long rows_q, long long rows_k, int d) {
+  Strides s;
+  s.q = s.o = s.dO = s.dq = contiguous(Hq, rows_q, d);
+  s.k = s.v = s.dk = s.dv = contiguous(Hkv, rows_k, d);
+  s.lse = contiguous(Hq, rows_q, 1);
+  return s;
+}
+
+Geo dense(int B, int Hq, int Hkv, int Nq, int Nkv, int d) {
+  return Geo{B, Hq, Hkv, Nq, Nkv, d, nullptr, nullptr, Nq, Nkv, contiguous_all(Hq, Hkv, Nq, Nkv, d)};
+}
 
 // Largest number of rows per head of a packed batch (keeps every TMA row
 // coordinate, start of a sequence plus a tile, inside int32).
 constexpr int kMaxTotal = 1 << 30;
+
+// Strides must be positive, and those of 16-bit tensors multiples of 8 elements
+// (16 bytes: TMA and the 16-byte loads and stores); a packed batch ignores the
+// batch stride.
+bool bad_str(const Str3& s, bool packed, int mult) {
+  if (s.h < 1 || s.n < 1 || s.h % mult || s.n % mult) return true;
+  if (!packed && (s.b < 1 || s.b % mult)) return true;
+  return s.h > (1LL << 36) || s.n > (1LL << 36) || (!packed && s.b > (1LL << 36));
+}
 
 int check_geo(const Geo& g, int dtype) {
   int st = check_shape(g.B, g.Hq, g.Hkv, g.Nq, g.Nkv, g.d, dtype);
@@ -135,6 +163,11 @@ int check_geo(const Geo& g, int dtype) {
     if ((reinterpret_cast<uintptr_t>(g.cu_q) & 3u) || (reinterpret_cast<uintptr_t>(g.cu_k) & 3u)) return FA_ERR_ALIGN;
     if (g.total_q < 1 || g.total_k < 1 || g.total_q > kMaxTotal || g.total_k > kMaxTotal) return FA_ERR_SHAPE;
   }
+  const bool pk = g.cu_q != nullptr;
+  const Strides& s = g.st;
+  for (const Str3* t : {&s.q, &s.k, &s.v, &s.o, &s.dO, &s.dq, &s.dk, &s.dv})
+    if (bad_str(*t, pk, 8)) return FA_ERR_ARG;
+  if (bad_str(s.lse, pk, 1)) return FA_ERR_ARG;
   return FA_OK;
 }
 
@@ -153,6 +186,7 @@ Problem make_problem(const Geo& g, float scale, int causal, int dtype, int deter
   pb.cu_k = g.cu_k;
   pb.total_q = g.rows_q();
   pb.total_k = g.rows_k();
+  pb.st = g.st;
   pb.bf16 = dtype == FA_BF16 ? 1 : 0;
   pb.deterministic = deterministic ? 1 : 0;
   return pb;
@@ -168,11 +202,17 @@ int check_ws(void* workspace, size_t bytes, const Geo& g, int deterministic) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 // Tensor maps of the Q-like and K-like tensors of a batch.
-int map_q(CUtensorMap* m, const void* p, int bf, const Geo& g, int box_rows) {
-  return make_map(m, p, bf, g.d, g.rows_q(), g.slabs_q(), box_rows);
+// A packed batch has one batch index; its (unused) batch stride is given a
+// valid value for the tensor map.
+Str3 map_strides(Str3 s, const Geo& g, int heads) {
+  if (g.cu_q) s.b = s.h * heads;
+  return s;
 }
-int map_k(CUtensorMap* m, const void* p, int bf, const Geo& g, int box_rows) {
-  return make_map(m, p, bf, g.d, g.rows_k(), g.slabs_k(), box_rows);
+int map_q(CUtensorMap* m, const void* p, const Str3& s, int bf, const Geo& g, int box_rows) {
+  return make_map(m, p, bf, g.d, g.rows_q(), g.Hq, g.batch(), map_strides(s, g, g.Hq), box_rows);
+}
+int map_k(CUtensorMap* m, const void* p, const Str3& s, int bf, const Geo& g, int box_rows) {
+  return make_map(m, p, bf, g.d, g.rows_k(), g.Hkv, g.batch(), map_strides(s, g, g.Hkv), box_rows);
 }
 
 int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, float* lse, float scale, int causal,
@@ -190,9 +230,9 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   if ((st = status_ptr(&status))) return st;
   CUtensorMap tq, tk, tv;
   const int bf = a.pb.bf16;
-  if ((st = map_q(&tq, q, bf, g, 128))) return st;
-  if ((st = map_k(&tk, k, bf, g, 128))) return st;
-  if ((st = map_k(&tv, v, bf, g, 128))) return st;
+  if ((st = map_q(&tq, q, g.st.q, bf, g, 128))) return st;
+  if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
+  if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
   return cuda_status(launch_fwd(a, tq, tk, tv, status, stream));
 }
 
@@ -229,10 +269,10 @@ int run_main(const Geo& g, const void* q, const void* k, const void* v, const vo
   if ((st = status_ptr(&a.status))) return st;
   CUtensorMap tq, tdo, tk, tv;
   const int bf = a.pb.bf16;
-  if ((st = map_q(&tq, q, bf, g, 64))) return st;
-  if ((st = map_q(&tdo, dO, bf, g, 64))) return st;
-  if ((st = map_k(&tk, k, bf, g, 128))) return st;
-  if ((st = map_k(&tv, v, bf, g, 128))) return st;
+  if ((st = map_q(&tq, q, g.st.q, bf, g, 64))) return st;
+  if ((st = map_q(&tdo, dO, g.st.dO, bf, g, 64))) return st;
+  if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
+  if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
   return cuda_status(launch_bwd_main(a, tq, tdo, tk, tv, stream));
 }
 
@@ -255,10 +295,10 @@ int run_dq(const Geo& g, const void* q, const void* k, const void* v, const void
   if ((st = get_encoder())) return st;
   CUtensorMap tq, tdo, tk, tv;
   const int bf = a.pb.bf16;
-  if ((st = map_q(&tq, q, bf, g, 128))) return st;
-  if ((st = map_q(&tdo, dO, bf, g, 128))) return st;
-  if ((st = map_k(&tk, k, bf, g, 128))) return st;
-  if ((st = map_k(&tv, v, bf, g, 128))) return st;
+  if ((st = map_q(&tq, q, g.st.q, bf, g, 128))) return st;
+  if ((st = map_q(&tdo, dO, g.st.dO, bf, g, 128))) return st;
+  if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
+  if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
   return cuda_status(launch_bwd_dq_det(a, tq, tdo, tk, tv, stream));
 }
 
@@ -282,7 +322,8 @@ int run_bwd(const Geo& g, const void* q, const void* k, const void* v, const voi
 
 Geo packed(int B, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k, int d, const int* cu_q,
            const int* cu_k) {
-  return Geo{B, Hq, Hkv, max_q, max_k, d, cu_q, cu_k, total_q, total_k};
+  return Geo{B, Hq, Hkv, max_q, max_k, d, cu_q, cu_k, total_q, total_k,
+             contiguous_all(Hq, Hkv, total_q, total_k, d)};
 }
 
 }  // namespace
@@ -366,6 +407,40 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
   if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
   return run_bwd(packed(B, Hq, Hkv, total_q, total_k, max_q, max_k, d, cu_seqlens_q, cu_seqlens_k), q, k, v, o,
                  dO, lse, dq, dk, dv, scale, causal, dtype, deterministic, workspace, workspace_bytes, stream);
+}
+
+namespace {
+Str3 to_str3(const fa_stride3& s) { return Str3{s.b, s.h, s.n}; }
+
+// Geometry of a strided call: dense (cu_q == NULL) or packed, with the given
+// strides or the contiguous ones.
+Geo strided_geo(const fa_strides* s, const int* cu_q, const int* cu_k, int B, int Hq, int Hkv, int Nq, int Nkv,
+                int total_q, int total_k, int d) {
+  Geo g = cu_q ? packed(B, Hq, Hkv, total_q, total_k, Nq, Nkv, d, cu_q, cu_k) : dense(B, Hq, Hkv, Nq, Nkv, d);
+  if (cu_q == nullptr && cu_k != nullptr) g.cu_k = cu_k;   // rejected by check_geo
+  if (s) {
+    g.st.q = to_str3(s->q); g.st.k = to_str3(s->k); g.st.v = to_str3(s->v);
+    g.st.o = to_str3(s->o); g.st.dO = to_str3(s->dO); g.st.dq = to_str3(s->dq);
+    g.st.dk = to_str3(s->dk); g.st.dv = to_str3(s->dv); g.st.lse = to_str3(s->lse);
+  }
+  return g;
+}
+}  // namespace
+
+int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, const fa_strides* strides,
+                   const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv, int Nq, int Nkv,
+                   int total_q, int total_k, int d, float scale, int causal, int dtype, cudaStream_t stream) {
+  return run_fwd(strided_geo(strides, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k, d), q, k,
+                 v, o, lse, scale, causal, dtype, stream);
+}
+
+int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, const fa_strides* strides, const int* cu_seqlens_q,
+                   const int* cu_seqlens_k, int B, int Hq, int Hkv, int Nq, int Nkv, int total_q, int total_k, int d,
+                   float scale, int causal, int dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  return run_bwd(strided_geo(strides, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k, d), q, k,
+                 v, o, dO, lse, dq, dk, dv, scale, causal, dtype, deterministic, workspace, workspace_bytes, stream);
 }
 
 int fa_last_device_error(cudaStream_t stream) {

@@ -56,13 +56,12 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
     const Seq sq = valid ? seq_of(m, b, status, 30) : Seq{0, 0, 0, 0, 0};
     const bool live = valid && r < sq.nq;
-    const long long qrow = live ? row_q(m, sq, b, h, r) : 0;
+    const long long qrow = sq.q_start + r;
     float acc = 0.f;
     if (live && 8 * sub < m.d) {
-      const long long src = qrow * (m.d / 8) + sub;
       float a[8], g[8];
-      widen8<BF16>(__ldg(o + src), a);
-      widen8<BF16>(__ldg(dO + src), g);
+      widen8<BF16>(__ldg(o + at(m.st.o, m, b, h, qrow) / 8 + sub), a);
+      widen8<BF16>(__ldg(dO + at(m.st.dO, m, b, h, qrow) / 8 + sub), g);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc = fmaf(a[i], g[i], acc);
     }
@@ -71,7 +70,7 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     if (!valid) continue;
     if (sub == 0) {
       Dv[row] = acc;
-      nLg[row] = live ? -lse[qrow] * 1.4426950408889634f : __int_as_float(0xff800000);
+      nLg[row] = live ? -lse[at(m.st.lse, m, b, h, qrow)] * 1.4426950408889634f : __int_as_float(0xff800000);
     }
     if (dq_acc != nullptr) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -106,7 +105,7 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
     out.y = pack2<BF16>(a.z * scale, a.w * scale);
     out.z = pack2<BF16>(c.x * scale, c.y * scale);
     out.w = pack2<BF16>(c.z * scale, c.w * scale);
-    dq[row_q(m, sq, b, h, r) * (m.d / 8) + c8] = out;
+    dq[at(m.st.dq, m, b, h, sq.q_start + r) / 8 + c8] = out;
   }
 }
 

@@ -109,8 +109,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const Seq sq = seq_of(p.m, b, p.status, 20);
-  const int zq = slab_q(p.m, b, h);                        // tensor-map slab of Q, dO
-  const int zk = slab_k(p.m, b, h / (p.Hq / p.Hkv));       // and of K, V
+  const int hk = h / (p.Hq / p.Hkv);                       // key/value head of the group
+  const int bc = bcoord(p.m, b);                           // batch coordinate in the tensor maps
   const int q0 = i * BQ;
   const int nKt = (sq.nk + BK - 1) / BK;
   const int qmax = min(q0 + BQ, sq.nq) - 1;
@@ -152,8 +152,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_arrive_expect_tx(bar(B_Q), 2 * L::TILE + 2 * BQ * 4);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
-        tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, zq);
-        tma_load_3d(sb + L::OFF_DO + hh * L::HALF, &tm_do, bar(B_Q), 64 * hh, sq.q_start + q0, zq);
+        tma_load_4d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, h, bc);
+        tma_load_4d(sb + L::OFF_DO + hh * L::HALF, &tm_do, bar(B_Q), 64 * hh, sq.q_start + q0, h, bc);
       }
       const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
       bulk_load(sb + L::OFF_LD, p.nLg + row, BQ * 4, bar(B_Q));
@@ -168,8 +168,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, zk);
-          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, zk);
+          tma_load_4d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
+          tma_load_4d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
         }
         issued = t + 1;
       }
@@ -299,7 +299,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
-    uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + row_q(p.m, sq, b, h, q) * p.m.d * 2;
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.dq) + at(p.m.st.dq, p.m, b, h, sq.q_start + q) * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 64; ++ch) {
       const int col = (D / 2) * grp + 32 * ch;

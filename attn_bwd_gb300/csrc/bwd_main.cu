@@ -202,12 +202,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0 && T > 0) {
-      const int kvh = slab_k(p.m, b, hkv);
+      const int bc = bcoord(p.m, b);                      // batch coordinate in the tensor maps
       mbar_arrive_expect_tx(bar(B_KV), 2 * L::KV_BYTES);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
-        tma_load_3d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(B_KV), 64 * hh, sq.k_start + kv0, kvh);
-        tma_load_3d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(B_KV), 64 * hh, sq.k_start + kv0, kvh);
+        tma_load_4d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(B_KV), 64 * hh, sq.k_start + kv0, hkv, bc);
+        tma_load_4d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(B_KV), 64 * hh, sq.k_start + kv0, hkv, bc);
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -217,13 +217,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int h = hkv * G + t / per_head;
         const int q0 = (i0 + t % per_head) * BM;
         const int bh = b * p.Hq + h;                      // workspace rows are (b, h, padded q)
-        const int zq = slab_q(p.m, b, h);
         const uint32_t fb = bar(B_QFULL + s);
         mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + L::LD_BYTES);
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_3d(sb + L::OFF_Q + s * L::Q_BYTES + hh * L::QHALF, &tm_q, fb, 64 * hh, sq.q_start + q0, zq);
-          tma_load_3d(sb + L::OFF_DO + s * L::Q_BYTES + hh * L::QHALF, &tm_do, fb, 64 * hh, sq.q_start + q0, zq);
+          tma_load_4d(sb + L::OFF_Q + s * L::Q_BYTES + hh * L::QHALF, &tm_q, fb, 64 * hh, sq.q_start + q0, h, bc);
+          tma_load_4d(sb + L::OFF_DO + s * L::Q_BYTES + hh * L::QHALF, &tm_do, fb, 64 * hh, sq.q_start + q0, h,
+                      bc);
         }
         const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
         bulk_load(sb + L::OFF_LD + s * L::LD_BYTES, p.nLg + row, BM * 4, fb);
@@ -484,7 +484,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int kv = kv0 + r;
     const float mul = is_dk ? p.scale : 1.0f;
     uint8_t* out = reinterpret_cast<uint8_t*>(is_dk ? p.dk : p.dv) +
-                   row_k(p.m, sq, b, hkv, kv) * p.m.d * 2;
+                   at(is_dk ? p.m.st.dk : p.m.st.dv, p.m, b, hkv, sq.k_start + kv) * 2;
     bool have = T > 0;
     if (have) {
       have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 13));

@@ -103,8 +103,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const Seq sq = seq_of(p.m, b, p.status, 50);
-  const int zq = slab_q(p.m, b, h);                        // tensor-map slab of Q, O
-  const int zk = slab_k(p.m, b, h / (p.Hq / p.Hkv));       // and of K, V
+  const int hk = h / (p.Hq / p.Hkv);                       // key/value head of the group
+  const int bc = bcoord(p.m, b);                           // batch coordinate in the tensor maps
   const int q0 = i * BQ;
   const int nKt = (sq.nk + BK - 1) / BK;
   const int qmax = min(q0 + BQ, sq.nq) - 1;
@@ -144,7 +144,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_arrive_expect_tx(bar(B_Q), L::TILE);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh)
-        tma_load_3d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, zq);
+        tma_load_4d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, h, bc);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % STAGES;
@@ -155,8 +155,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_3d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, zk);
-          tma_load_3d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, zk);
+          tma_load_4d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
+          tma_load_4d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
         }
         issued = t + 1;
       }
@@ -297,8 +297,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     const bool aborted = *abort_flag != 0;
     const float inv = l > 0.f ? 1.f / l : 0.f;         // a row that saw no key: O = 0
-    const long long orow = row_q(p.m, sq, b, h, q);
-    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + orow * p.m.d * 2;
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + at(p.m.st.o, p.m, b, h, sq.q_start + q) * 2;
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t pk[16];
@@ -321,7 +320,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
     }
     if (q < sq.nq && !aborted)
-      p.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+      p.lse[at(p.m.st.lse, p.m, b, h, sq.q_start + q)] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
   }
 
   tc_fence_before();

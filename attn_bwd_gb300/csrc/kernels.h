@@ -21,6 +21,16 @@ struct Workspace {
   float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
 };
 
+// Element strides of a tensor's batch, head and row axes (its d axis is contiguous).
+struct Str3 {
+  long long b, h, n;
+};
+
+// Strides of every tensor of a problem.
+struct Strides {
+  Str3 q, k, v, o, dO, dq, dk, dv, lse;
+};
+
 // Geometry of the batch, passed to every kernel (see seq.cuh).
 struct SeqMap {
   const int* cu_q;   // packed batch: [B + 1] query offsets (device); nullptr for a dense batch
@@ -30,6 +40,7 @@ struct SeqMap {
   int Nq, Nkv;       // dense: the lengths; packed: the longest lengths
   int total_q, total_k;  // packed: rows per head
   int causal_mode;   // 0 none, 1 top-left, 2 bottom-right
+  Strides st;
 };
 
 struct Problem {
@@ -43,6 +54,7 @@ struct Problem {
   const int* cu_q;   // packed batch offsets, or nullptr
   const int* cu_k;
   int total_q, total_k;
+  Strides st;
 };
 
 inline SeqMap seq_map(const Problem& pb) {
@@ -54,6 +66,7 @@ inline SeqMap seq_map(const Problem& pb) {
   m.Nq = pb.Nq; m.Nkv = pb.Nkv;
   m.total_q = pb.total_q; m.total_k = pb.total_k;
   m.causal_mode = pb.causal_mode;
+  m.st = pb.st;
   return m;
 }
 

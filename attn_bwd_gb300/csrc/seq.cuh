@@ -1,15 +1,16 @@
 // seq.cuh -- where sequence b of a batch lives, for dense and packed batches.
 //
-// Dense batch:  Q-like tensors [B, Hq, Nq, d], K-like [B, Hkv, Nkv, d]; every
-//               sequence has Nq queries and Nkv keys.
+// Dense batch:  Q-like tensors [B, Hq, Nq, d], K-like [B, Hkv, Nkv, d] (any
+//               strides); every sequence has Nq queries and Nkv keys.
 // Packed batch: Q-like tensors [Hq, total_q, d], K-like [Hkv, total_k, d];
 //               sequence b owns rows [cu_q[b], cu_q[b+1]) of every query head
 //               and [cu_k[b], cu_k[b+1]) of every key/value head, and attends
 //               only within itself.  Nq / Nkv then hold the longest lengths,
 //               which size the grids and the padded workspace rows.
-// The kernels address a head's rows as one "slab" of a 3-D view
-// (d, rows, slabs): slab b*H + h of Nq rows (dense) or slab h of total rows
-// starting at row cu[b] (packed).  Tensor maps use the same view.
+// Every tensor is addressed through its own element strides for the batch,
+// head and row axes (the d axis is contiguous), and through a 4-D tensor map
+// (d, rows, heads, batch) built on the same strides.  A packed batch has a
+// batch extent of 1; its sequence b starts at row cu[b] of every head.
 #pragma once
 
 #include <cstdint>
@@ -56,21 +57,14 @@ __device__ __forceinline__ Seq seq_of(const SeqMap& m, int b, unsigned int* stat
   return s;
 }
 
-// Slab index of query head h of sequence b in Q-like tensors, and of key/value
-// head hk in K-like tensors.
-__device__ __forceinline__ int slab_q(const SeqMap& m, int b, int h) { return m.cu_q ? h : b * m.Hq + h; }
-__device__ __forceinline__ int slab_k(const SeqMap& m, int b, int hk) { return m.cu_q ? hk : b * m.Hkv + hk; }
+// Batch coordinate of sequence b in tensor maps and addresses (a packed batch
+// has one: its sequences are told apart by their rows).
+__device__ __forceinline__ int bcoord(const SeqMap& m, int b) { return m.cu_q ? 0 : b; }
 
-// Rows per slab.
-__device__ __forceinline__ long long slab_rows_q(const SeqMap& m) { return m.cu_q ? m.total_q : m.Nq; }
-__device__ __forceinline__ long long slab_rows_k(const SeqMap& m) { return m.cu_q ? m.total_k : m.Nkv; }
-
-// Row index (into [slabs * rows]) of query r of head h of sequence s (b), and of key r.
-__device__ __forceinline__ long long row_q(const SeqMap& m, const Seq& s, int b, int h, int r) {
-  return static_cast<long long>(slab_q(m, b, h)) * slab_rows_q(m) + s.q_start + r;
-}
-__device__ __forceinline__ long long row_k(const SeqMap& m, const Seq& s, int b, int hk, int r) {
-  return static_cast<long long>(slab_k(m, b, hk)) * slab_rows_k(m) + s.k_start + r;
+// Element offset of row `row` of head h of sequence b in a tensor with strides s
+// (row already includes the sequence's first row).
+__device__ __forceinline__ long long at(const Str3& s, const SeqMap& m, int b, int h, long long row) {
+  return static_cast<long long>(bcoord(m, b)) * s.b + static_cast<long long>(h) * s.h + row * s.n;
 }
 
 }  // namespace fa

@@ -129,3 +129,58 @@ def backward_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale: float, causal, deter
     _check(_lib.fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, dq_, dk_, B, Hq, Hkv, total_q, total_k, max_q, max_k,
                               d, scale, causal, _DT[q.dtype], int(deterministic), ws, n, s), "fa_bwd_varlen")
     return dq, dk, dv
+
+
+# ------------------------------------------------------------ strided tensors
+
+def _str3(t):
+    """(b, h, n) element strides of a [B, H, N, d] view, or of a [H, N] / [B, H, N] L."""
+    st = t.stride()
+    if t.dim() == 4:
+        return st[0], st[1], st[2]
+    if t.dim() == 3:
+        return st[0], st[1], st[2]
+    raise ValueError("expected a 3-D or 4-D tensor")
+
+
+def _need_rows(*ts):
+    for t in ts:
+        if not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("tensors must be CUDA tensors with a contiguous last (d) axis")
+
+
+def forward_strided(q, k, v, scale: float, causal, stream=None):
+    """Forward on [B, H, N, d] views with any strides (d contiguous), e.g. transposes of
+    [B, N, H, d] tensors.  O is allocated with q's strides; L is contiguous [B, Hq, Nq]."""
+    _need_rows(q, k, v)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    st = _lib.make_strides(q=_str3(q), k=_str3(k), v=_str3(v), o=_str3(o), dO=_str3(q), dq=_str3(q), dk=_str3(k),
+                           dv=_str3(k), lse=_str3(lse))
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_fwd_strided(q, k, v, o, lse, st, None, None, B, Hq, Hkv, Nq, Nkv, 0, 0, d, scale, causal,
+                               _DT[q.dtype], s), "fa_fwd_strided")
+    return o, lse
+
+
+def backward_strided(q, k, v, o, do, lse, scale: float, causal, deterministic: bool = False, out=None, stream=None):
+    """Backward on [B, H, N, d] views with any strides (d contiguous); dQ, dK, dV are allocated
+    like q, k, v unless ``out`` is given."""
+    _need_rows(q, k, v, o, do)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    st = _lib.make_strides(q=_str3(q), k=_str3(k), v=_str3(v), o=_str3(o), dO=_str3(do), dq=_str3(dq),
+                           dk=_str3(dk), dv=_str3(dv), lse=_str3(lse))
+    n = _lib.fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, int(deterministic))
+    if n == 0:
+        raise ValueError("invalid shape for the backward")
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_bwd_strided(q, k, v, o, do, lse, dq, dk, dv, st, None, None, B, Hq, Hkv, Nq, Nkv, 0, 0, d, scale,
+                               causal, _DT[q.dtype], int(deterministic), ws, n, s), "fa_bwd_strided")
+    return dq, dk, dv

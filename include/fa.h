@@ -229,6 +229,47 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
                   int d, float scale, int causal, int dtype, int deterministic,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Strided tensors.  The Triton kernel of "Extra transposes cause 8x speedup for
+ * sequence-parallel Flash Attention backward" (triton #1806, "Minimal Repro")
+ * takes batch, head, row and column strides for every tensor; these entry
+ * points take the batch, head and row strides, in ELEMENTS, of every tensor
+ * (the d axis must be contiguous), so that e.g. [B, N, H, d] tensors or a
+ * token-major packed batch [total, H, d] are used in place.
+ * Strides must be positive; those of the 16-bit tensors multiples of 8 (16
+ * bytes); a packed batch ignores the batch strides.  Tensors must not overlap.
+ * Bad strides: FA_ERR_ARG.
+ */
+typedef struct {
+  long long b, h, n;   /* element strides of the batch, head and row axes */
+} fa_stride3;
+
+typedef struct {
+  fa_stride3 q, k, v, o, dO, dq, dk, dv;   /* 16-bit tensors */
+  fa_stride3 lse;                          /* fp32 L */
+} fa_strides;
+
+/*
+ * fa_fwd_strided / fa_bwd_strided -- the general forms of fa_fwd / fa_bwd and
+ * of their packed-batch variants.  strides: NULL means contiguous ([B, H, N, d]
+ * dense, [H, total, d] packed).  cu_seqlens_q == NULL (and cu_seqlens_k ==
+ * NULL): a dense batch of B sequences of Nq queries and Nkv keys (total_q,
+ * total_k ignored).  Otherwise a packed batch as for fa_fwd_varlen: Nq, Nkv
+ * are the longest lengths and the row axes hold total_q / total_k rows.
+ * Workspace: fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, deterministic).
+ */
+int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                   const fa_strides* strides, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                   int B, int Hq, int Hkv, int Nq, int Nkv, int total_q, int total_k, int d,
+                   float scale, int causal, int dtype, cudaStream_t stream);
+
+int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   const fa_strides* strides, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                   int B, int Hq, int Hkv, int Nq, int Nkv, int total_q, int total_k, int d,
+                   float scale, int causal, int dtype, int deterministic,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of an fa_status value (static string, never NULL). */
 const char* fa_strerror(int status);
 

@@ -164,3 +164,31 @@ def test_varlen_workspace_matches_dense_at_the_longest_length(lib):
     for det in (0, 1):
         assert (_lib.fa_bwd_varlen_workspace_size(3, 4, 2, 300, 200, 128, det)
                 == _lib.fa_bwd_workspace_size(3, 4, 2, 300, 200, 128, det))
+
+
+def _st(**over):
+    base = dict(q=(4096, 1024, 64), k=(2048, 1024, 64), v=(2048, 1024, 64), o=(4096, 1024, 64),
+                dO=(4096, 1024, 64), dq=(4096, 1024, 64), dk=(2048, 1024, 64), dv=(2048, 1024, 64),
+                lse=(64, 16, 1))
+    base.update(over)
+    return _lib.make_strides(**base)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(), None),
+    (dict(q=(4096, 1024, 60)), _lib.FA_ERR_ARG),          # row stride not a multiple of 8 elements
+    (dict(dk=(2048, 0, 64)), _lib.FA_ERR_ARG),            # zero head stride
+    (dict(o=(-4096, 1024, 64)), _lib.FA_ERR_ARG),         # negative batch stride
+    (dict(lse=(64, 16, 0)), _lib.FA_ERR_ARG),             # zero row stride of L
+])
+def test_bwd_strided_validates_strides(lib, over, code):
+    st = _st(**over)
+    # a workspace that is too small makes the valid layout stop at the workspace check instead
+    r = _lib.fa_bwd_strided(A, A, A, A, A, A, A, A, A, st, None, None, 1, 2, 1, 16, 16, 0, 0, 64, 0.1, 0,
+                            _lib.FA_BF16, 0, W, 16)
+    assert r == (code if code is not None else _lib.FA_ERR_WORKSPACE)
+
+
+def test_strided_offsets_must_come_in_pairs(lib):
+    r = _lib.fa_fwd_strided(A, A, A, A, A, None, None, C, 1, 2, 1, 16, 16, 16, 16, 64, 0.1, 0, _lib.FA_BF16)
+    assert r == _lib.FA_ERR_NULL
