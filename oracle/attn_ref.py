@@ -80,14 +80,19 @@ def causal_delta(causal, nq: int, nk: int):
     raise ValueError(f"unknown causal mode {causal!r}")
 
 
-def scores(q: np.ndarray, k: np.ndarray, scale: float, causal) -> np.ndarray:
-    """S = scale * Q K^T for one head, [Nq, Nkv], with the causal mask applied.
+def scores(q: np.ndarray, k: np.ndarray, scale: float, causal, bias=None) -> np.ndarray:
+    """S = scale * Q K^T (+ bias) for one head, [Nq, Nkv], with the causal mask applied.
 
     Top-left drops key j for query i whenever j > i (the literal rule of the
     pages' CUDA kernel); bottom-right whenever j > i + Nkv - Nq.  With
-    Nq == Nkv both are the usual mask.
+    Nq == Nkv both are the usual mask.  ``bias`` [Nq, Nkv] is added to the
+    scaled scores before masking ("[Kernel] Flash attention 2", "Details":
+    attention bias and attention masking); a boolean mask is the bias -inf
+    at the dropped positions.
     """
     s = scale * (q @ k.T)
+    if bias is not None:
+        s = s + bias
     nq, nk = s.shape
     delta = causal_delta(causal, nq, nk)
     if delta is not None:
@@ -119,26 +124,27 @@ def probs(s: np.ndarray, lse: np.ndarray) -> np.ndarray:
     return p
 
 
-def head_forward(q, k, v, scale, causal):
+def head_forward(q, k, v, scale, causal, bias=None):
     """Forward for one head: returns (O [Nq,d], L [Nq], P [Nq,Nkv])."""
-    s = scores(q, k, scale, causal)
+    s = scores(q, k, scale, causal, bias)
     lse = logsumexp_rows(s)
     p = probs(s, lse)
     return p @ v, lse, p
 
 
-def head_backward(q, k, v, do, scale, causal, lse=None, o=None):
+def head_backward(q, k, v, do, scale, causal, lse=None, o=None, bias=None):
     """Backward for one head.
 
     Returns a dict with dq [Nq,d], dk [Nkv,d], dv [Nkv,d], D [Nq] (the
     rowsum(P * dP) form), D_rowdot [Nq] (the rowsum(dO * O) form, only when
-    ``o`` is given or computed), and dS [Nq,Nkv].
+    ``o`` is given or computed), and dS [Nq,Nkv], which is also the gradient of
+    the loss with respect to an additive bias (the bias enters S with weight 1).
 
     ``lse`` / ``o``: when given, P is formed from that log-sum-exp and
     D_rowdot from that output (used to isolate the backward from forward
     rounding); otherwise both are recomputed here in fp64.
     """
-    s = scores(q, k, scale, causal)
+    s = scores(q, k, scale, causal, bias)
     if lse is None:
         lse = logsumexp_rows(s)
     p = probs(s, lse)
@@ -154,9 +160,20 @@ def head_backward(q, k, v, do, scale, causal, lse=None, o=None):
     return {"dq": dq, "dk": dk, "dv": dv, "D": D, "D_rowdot": D_rowdot, "dS": ds, "P": p}
 
 
-def forward(q, k, v, scale: float, causal: bool):
-    """Full forward over [B, Hq, Nq, d] / [B, Hkv, Nkv, d].  Returns (O, L) in fp64."""
+def _bias_of(bias, b, h):
+    """The [Nq, Nkv] bias of (b, h) from a [B or 1, Hq or 1, Nq, Nkv] array (size-1 axes broadcast)."""
+    if bias is None:
+        return None
+    return bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0]
+
+
+def forward(q, k, v, scale: float, causal: bool, bias=None):
+    """Full forward over [B, Hq, Nq, d] / [B, Hkv, Nkv, d].  Returns (O, L) in fp64.
+
+    ``bias``: optional additive bias [B or 1, Hq or 1, Nq, Nkv] (size-1 axes broadcast).
+    """
     q, k, v = _f64(q), _f64(k), _f64(v)
+    bias = None if bias is None else _f64(bias)
     B, Hq, Nq, d = q.shape
     Hkv = k.shape[1]
     o = np.zeros((B, Hq, Nq, d))
@@ -164,12 +181,13 @@ def forward(q, k, v, scale: float, causal: bool):
     for b in range(B):
         for h in range(Hq):
             hk = kv_head(h, Hq, Hkv)
-            o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, hk], v[b, hk], scale, causal)
+            o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, hk], v[b, hk], scale, causal, _bias_of(bias, b, h))
     return o, lse
 
 
-def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=None):
-    """Full backward.  Returns dict of fp64 arrays dq, dk, dv, D, D_rowdot.
+def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=None, bias=None):
+    """Full backward.  Returns dict of fp64 arrays dq, dk, dv, D, D_rowdot, and dbias
+    [B, Hq, Nq, Nkv] (= dS of every head) when ``bias`` is given.
 
     ``groups``: optional iterable of (b, h_kv) pairs; when given only those
     groups are computed (their query heads' dq/D and the group's dk/dv), the
@@ -178,6 +196,7 @@ def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=N
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     lse = None if lse is None else _f64(lse)
     o = None if o is None else _f64(o)
+    bias = None if bias is None else _f64(bias)
     B, Hq, Nq, d = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
     G = Hq // Hkv
@@ -189,6 +208,7 @@ def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=N
     dv = np.full((B, Hkv, Nkv, d), fill)
     D = np.full((B, Hq, Nq), fill)
     D_rowdot = np.full((B, Hq, Nq), fill)
+    dbias = np.full((B, Hq, Nq, Nkv), fill) if bias is not None else None
     todo = groups if groups is not None else [(b, g) for b in range(B) for g in range(Hkv)]
     for b, g in todo:
         dk[b, g] = 0.0
@@ -196,13 +216,18 @@ def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=N
         for h in range(g * G, (g + 1) * G):
             r = head_backward(q[b, h], k[b, g], v[b, g], do[b, h], scale, causal,
                               None if lse is None else lse[b, h],
-                              None if o is None else o[b, h])
+                              None if o is None else o[b, h], _bias_of(bias, b, h))
+            if dbias is not None:
+                dbias[b, h] = r["dS"]
             dq[b, h] = r["dq"]
             dk[b, g] += r["dk"]
             dv[b, g] += r["dv"]
             D[b, h] = r["D"]
             D_rowdot[b, h] = r["D_rowdot"]
-    return {"dq": dq, "dk": dk, "dv": dv, "D": D, "D_rowdot": D_rowdot}
+    out = {"dq": dq, "dk": dk, "dv": dv, "D": D, "D_rowdot": D_rowdot}
+    if dbias is not None:
+        out["dbias"] = dbias
+    return out
 
 
 def backward_flops(B, Hq, Nq, Nkv, d, causal) -> float:

@@ -498,3 +498,73 @@ def test_pins_catch_keys_leaking_across_sequences(monkeypatch):
         monkeypatch.setattr(attn_ref, fn, ns[fn])
     with pytest.raises(AssertionError):
         test_varlen_matches_torch_sdpa_on_the_packed_sequence(0)
+
+
+# ------------------------------------------------------ additive bias
+
+@pytest.mark.parametrize("bshape,causal", [
+    ((2, 4), 0), ((1, 4), 1), ((2, 1), 2), ((1, 1), 0),
+])
+def test_bias_matches_torch_sdpa_float_mask(bshape, causal):
+    """torch's fp64 SDPA adds a float attn_mask to the scaled scores and differentiates it:
+    an independent derivation of O and of dBias (= dS) for every broadcast shape."""
+    B, Hq, Hkv, Nq, Nkv, d = 2, 4, 2, 11, 19, 8
+    g = torch.Generator().manual_seed(51 + causal)
+    q = torch.randn(B, Hq, Nq, d, generator=g, dtype=torch.float64)
+    k = torch.randn(B, Hkv, Nkv, d, generator=g, dtype=torch.float64)
+    v = torch.randn(B, Hkv, Nkv, d, generator=g, dtype=torch.float64)
+    do = torch.randn(B, Hq, Nq, d, generator=g, dtype=torch.float64)
+    bias = torch.randn(bshape[0], bshape[1], Nq, Nkv, generator=g, dtype=torch.float64)
+    scale = 0.45
+    mask = bias.clone()
+    delta = attn_ref.causal_delta(causal, Nq, Nkv)
+    if delta is not None:
+        allowed = torch.ones(Nq, Nkv, dtype=torch.bool).tril(diagonal=delta)
+        mask = mask.masked_fill(~allowed, float("-inf"))
+    tq, tk, tv, tb = (t.clone().requires_grad_(True) for t in (q, k, v, bias))
+    tm = tb if delta is None else tb.masked_fill(~allowed, float("-inf"))
+    rep = Hq // Hkv
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(rep, dim=1), tv.repeat_interleave(rep, dim=1), attn_mask=tm, scale=scale)
+    out.backward(do)
+    o, _ = attn_ref.forward(q, k, v, scale, causal, bias=bias)
+    r = attn_ref.backward(q, k, v, do, scale, causal, bias=bias)
+    np.testing.assert_allclose(o, out.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dq"], tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dk"], tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(r["dv"], tv.grad.numpy(), atol=1e-12)
+    # dBias of a broadcast bias is dS summed over the broadcast axes
+    db = r["dbias"]
+    if bshape[0] == 1:
+        db = db.sum(axis=0, keepdims=True)
+    if bshape[1] == 1:
+        db = db.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(db, tb.grad.numpy(), atol=1e-12)
+
+
+def test_minus_inf_bias_is_a_mask():
+    """A -inf bias drops keys: equal to removing them, and a row with every key dropped
+    sees none (O = 0, L = -inf)."""
+    rng = np.random.default_rng(61)
+    q, do = _rand((1, 2, 6, 4), rng), _rand((1, 2, 6, 4), rng)
+    k, v = _rand((1, 1, 9, 4), rng), _rand((1, 1, 9, 4), rng)
+    keep = np.array([1, 0, 1, 1, 0, 0, 1, 0, 1], dtype=bool)
+    bias = np.where(keep, 0.0, -np.inf)[None, None, None, :].repeat(6, axis=2)
+    bias[0, 0, 3, :] = -np.inf
+    o, lse = attn_ref.forward(q, k, v, 0.5, 0, bias=bias)
+    o2, lse2 = attn_ref.forward(q, k[:, :, keep], v[:, :, keep], 0.5, 0)
+    rows = [0, 1, 2, 4, 5]          # row 3 drops every key (the bias broadcasts over both heads)
+    np.testing.assert_allclose(o[0, :, rows], o2[0, :, rows], atol=1e-14)
+    assert (o[0, :, 3] == 0).all() and np.isneginf(lse[0, :, 3]).all()
+    r = attn_ref.backward(q, k, v, do, 0.5, 0, bias=bias)
+    assert (r["dq"][0, :, 3] == 0).all()
+    assert (r["dk"][0, 0, ~keep] == 0).all() and (r["dbias"][..., ~keep] == 0).all()
+
+
+def test_pins_catch_bias_scaled_by_the_softmax_scale(monkeypatch):
+    src = inspect.getsource(attn_ref.scores)
+    ns = dict(attn_ref.__dict__)
+    exec(src.replace("s = s + bias", "s = s + scale * bias"), ns)
+    monkeypatch.setattr(attn_ref, "scores", ns["scores"])
+    with pytest.raises(AssertionError):
+        test_bias_matches_torch_sdpa_float_mask((2, 4), 0)
