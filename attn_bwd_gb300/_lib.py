@@ -40,6 +40,11 @@ class fa_strides(ctypes.Structure):
     _fields_ = [(n, fa_stride3) for n in ("q", "k", "v", "o", "dO", "dq", "dk", "dv", "lse")]
 
 
+class fa_bias(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("bias_strides", fa_stride3), ("dbias", ctypes.c_void_p),
+                ("dbias_strides", fa_stride3)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
@@ -64,6 +69,10 @@ _SIGNATURES = {
                             _F, _I, _I, _P]),
     "fa_bwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(fa_strides), _P, _P, _I, _I, _I, _I,
                             _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
+    "fa_fwd_bias": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(fa_bias), ctypes.POINTER(fa_strides), _P, _P, _I, _I,
+                         _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_bwd_bias": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(fa_bias), ctypes.POINTER(fa_strides),
+                         _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
 }
 
 FA_STATIC_SCRATCH_BYTES = 64 << 20
@@ -204,3 +213,28 @@ def fa_bwd_strided(q, k, v, o, dO, lse, dq, dk, dv, strides, cu_q, cu_k, B, Hq, 
                                  _ptr(dv), sp, _ptr(cu_q), _ptr(cu_k), B, Hq, Hkv, Nq, Nkv, total_q, total_k, d,
                                  float(scale), int(causal), int(dtype), int(deterministic), _ptr(workspace),
                                  int(workspace_bytes), _stream(stream))
+
+
+def make_bias(bias, bias_strides, dbias=None, dbias_strides=(0, 0, 0)) -> fa_bias:
+    """fa_bias from a bias pointer and its (b, h, q) element strides (0 broadcasts), and an optional dBias."""
+    return fa_bias(_ptr(bias), fa_stride3(*[int(x) for x in bias_strides]), _ptr(dbias),
+                   fa_stride3(*[int(x) for x in dbias_strides]))
+
+
+def fa_fwd_bias(q, k, v, o, lse, bias, strides, cu_q, cu_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k, d, scale, causal,
+                dtype, stream=None) -> int:
+    bp = ctypes.byref(bias) if bias is not None else None
+    sp = ctypes.byref(strides) if strides is not None else None
+    return load().fa_fwd_bias(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), bp, sp, _ptr(cu_q), _ptr(cu_k), B, Hq,
+                              Hkv, Nq, Nkv, total_q, total_k, d, float(scale), int(causal), int(dtype),
+                              _stream(stream))
+
+
+def fa_bwd_bias(q, k, v, o, dO, lse, dq, dk, dv, bias, strides, cu_q, cu_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k, d,
+                scale, causal, dtype, deterministic, workspace, workspace_bytes, stream=None) -> int:
+    bp = ctypes.byref(bias) if bias is not None else None
+    sp = ctypes.byref(strides) if strides is not None else None
+    return load().fa_bwd_bias(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                              bp, sp, _ptr(cu_q), _ptr(cu_k), B, Hq, Hkv, Nq, Nkv, total_q, total_k, d, float(scale),
+                              int(causal), int(dtype), int(deterministic), _ptr(workspace), int(workspace_bytes),
+                              _stream(stream))

@@ -120,6 +120,10 @@ struct Geo {
   const int* cu_k;
   int total_q, total_k;
   Strides st;        // element strides of every tensor
+  const void* bias = nullptr;   // optional additive bias and its gradient (see fa_bias)
+  Str3 bias_st{0, 0, 0};
+  void* dbias = nullptr;
+  Str3 dbias_st{0, 0, 0};
   int batch() const { return cu_q ? 1 : B; }
   int rows_q() const { return cu_q ? total_q : Nq; }
   int rows_k() const { return cu_q ? total_k : Nkv; }
@@ -168,6 +172,17 @@ int check_geo(const Geo& g, int dtype) {
   for (const Str3* t : {&s.q, &s.k, &s.v, &s.o, &s.dO, &s.dq, &s.dk, &s.dv})
     if (bad_str(*t, pk, 8)) return FA_ERR_ARG;
   if (bad_str(s.lse, pk, 1)) return FA_ERR_ARG;
+  if (g.dbias != nullptr && g.bias == nullptr) return FA_ERR_NULL;
+  if (g.bias != nullptr) {
+    if (misaligned(g.bias)) return FA_ERR_ALIGN;
+    const Str3& b = g.bias_st;        // 0 broadcasts; otherwise whole 16-byte pieces
+    if (b.b < 0 || b.h < 0 || b.n < 0 || b.b % 8 || b.h % 8 || b.n % 8) return FA_ERR_ARG;
+  }
+  if (g.dbias != nullptr) {
+    if (misaligned(g.dbias)) return FA_ERR_ALIGN;
+    const Str3& b = g.dbias_st;       // every (b, h, q) row its own
+    if (b.b < 1 || b.h < 1 || b.n < 1 || b.b % 8 || b.h % 8 || b.n % 8) return FA_ERR_ARG;
+  }
   return FA_OK;
 }
 
@@ -187,6 +202,10 @@ Problem make_problem(const Geo& g, float scale, int causal, int dtype, int deter
   pb.total_q = g.rows_q();
   pb.total_k = g.rows_k();
   pb.st = g.st;
+  pb.bias = g.bias;
+  pb.bias_st = g.bias_st;
+  pb.dbias = g.dbias;
+  pb.dbias_st = g.dbias_st;
   pb.bf16 = dtype == FA_BF16 ? 1 : 0;
   pb.deterministic = deterministic ? 1 : 0;
   return pb;
@@ -273,6 +292,8 @@ int run_main(const Geo& g, const void* q, const void* k, const void* v, const vo
   if ((st = map_q(&tdo, dO, g.st.dO, bf, g, 64))) return st;
   if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
   if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
+  if (a.pb.dbias != nullptr && a.pb.causal)
+    if ((st = cuda_status(launch_dbias_zero(a.pb, a.status, stream)))) return st;
   return cuda_status(launch_bwd_main(a, tq, tdo, tk, tv, stream));
 }
 
@@ -425,7 +446,41 @@ Geo strided_geo(const fa_strides* s, const int* cu_q, const int* cu_k, int B, in
   }
   return g;
 }
+
+// Adds the bias of an fa_bias description to a geometry.
+Geo with_bias(Geo g, const fa_bias* bias) {
+  if (bias) {
+    g.bias = bias->bias;
+    g.bias_st = to_str3(bias->bias_strides);
+    g.dbias = bias->dbias;
+    g.dbias_st = to_str3(bias->dbias_strides);
+  }
+  return g;
+}
 }  // namespace
+
+int fa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, const fa_bias* bias,
+                const fa_strides* strides, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv,
+                int Nq, int Nkv, int total_q, int total_k, int d, float scale, int causal, int dtype,
+                cudaStream_t stream) {
+  if (bias != nullptr && bias->bias == nullptr) return FA_ERR_NULL;
+  if (bias != nullptr && bias->dbias != nullptr) return FA_ERR_ARG;   // the forward writes no dBias
+  return run_fwd(with_bias(strided_geo(strides, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k,
+                                       d), bias),
+                 q, k, v, o, lse, scale, causal, dtype, stream);
+}
+
+int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                void* dq, void* dk, void* dv, const fa_bias* bias, const fa_strides* strides,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv, int Nq, int Nkv,
+                int total_q, int total_k, int d, float scale, int causal, int dtype, int deterministic,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (bias != nullptr && bias->bias == nullptr) return FA_ERR_NULL;
+  return run_bwd(with_bias(strided_geo(strides, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, Nq, Nkv, total_q, total_k,
+                                       d), bias),
+                 q, k, v, o, dO, lse, dq, dk, dv, scale, causal, dtype, deterministic, workspace, workspace_bytes,
+                 stream);
+}
 
 int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, const fa_strides* strides,
                    const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv, int Nq, int Nkv,

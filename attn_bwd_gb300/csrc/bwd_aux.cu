@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <math_constants.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -70,7 +71,10 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     if (!valid) continue;
     if (sub == 0) {
       Dv[row] = acc;
-      nLg[row] = live ? -lse[at(m.st.lse, m, b, h, qrow)] * 1.4426950408889634f : __int_as_float(0xff800000);
+      // -L * log2(e); -inf on padding rows and on rows that see no key (L = -inf), so
+      // that every exponent of such a row is -inf whatever the scores and bias are
+      const float L = live ? lse[at(m.st.lse, m, b, h, qrow)] : -CUDART_INF_F;
+      nLg[row] = L == -CUDART_INF_F ? -CUDART_INF_F : -L * 1.4426950408889634f;
     }
     if (dq_acc != nullptr) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -132,6 +136,40 @@ __global__ void wait_selftest_kernel(unsigned int* status, long long timeout_ns)
   __syncthreads();
 }
 
+// dBias of a causal problem: the main kernel visits, for KV tile j, only the
+// query tiles from i0(j) = max(0, j*BN - delta) / BM on and writes dS there;
+// every key of the tiles it skips is masked for those queries, so dBias is 0.
+// Query row q (tile qt = q / BM) is skipped exactly for the KV tiles j with
+// i0(j) > qt, i.e. j*BN >= (qt + 1)*BM + delta: keys from
+// jmin*BN = ceil(((qt + 1)*BM + delta) / BN) * BN to the end of the row.
+// One thread writes 8 keys (16 bytes) of one row.
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+dbias_zero_kernel(SeqMap m, long long rows, int kchunks, unsigned int* status) {
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < rows * kchunks;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = idx / kchunks;                  // (b, h, q) with q < Nq (the longest length)
+    const int c8 = static_cast<int>(idx - row * kchunks);
+    const int q = static_cast<int>(row % m.Nq);
+    const long long bh = row / m.Nq;
+    const int b = static_cast<int>(bh / m.Hq);
+    const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
+    const Seq sq = seq_of(m, b, status, 32);
+    if (q >= sq.nq) continue;
+    const long long first = static_cast<long long>(q / kMainBM + 1) * kMainBM + sq.delta;
+    const long long jmin = first <= 0 ? 0 : (first + kMainBN - 1) / kMainBN;
+    const long long kv = 8LL * c8;
+    if (kv + 8 <= jmin * kMainBN || kv >= sq.nk) continue;
+    uint16_t* dst = static_cast<uint16_t*>(m.dbias) + bias_row(m.dbias_st, b, h, q);
+    if (kv >= jmin * kMainBN && kv + 8 <= sq.nk) {
+      *reinterpret_cast<uint4*>(dst + kv) = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      for (long long e = kv; e < kv + 8 && e < sq.nk; ++e)
+        if (e >= jmin * kMainBN) dst[e] = 0;
+    }
+  }
+}
+
 long long grid_for(long long work_items, int per_block) {
   long long g = (work_items + per_block - 1) / per_block;
   const long long cap = static_cast<long long>(kSMs) * 16;
@@ -176,6 +214,17 @@ cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, 
   if (pb.d > 64)
     return pb.bf16 ? conv_t<128, true>(pb, ws, dq, status, stream) : conv_t<128, false>(pb, ws, dq, status, stream);
   return pb.bf16 ? conv_t<64, true>(pb, ws, dq, status, stream) : conv_t<64, false>(pb, ws, dq, status, stream);
+}
+
+cudaError_t launch_dbias_zero(const Problem& pb, unsigned int* status, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.Nq;
+  const int kchunks = (pb.Nkv + 7) / 8;
+  const long long grid = grid_for(rows * kchunks, 256);
+  if (pb.bf16)
+    dbias_zero_kernel<true><<<static_cast<unsigned>(grid), 256, 0, stream>>>(seq_map(pb), rows, kchunks, status);
+  else
+    dbias_zero_kernel<false><<<static_cast<unsigned>(grid), 256, 0, stream>>>(seq_map(pb), rows, kchunks, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cudaStream_t stream) {

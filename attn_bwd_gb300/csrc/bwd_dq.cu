@@ -83,7 +83,7 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -240,6 +240,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tdP = tmem + lane_off + L::COL_DP + 64 * grp;
     const int q = q0 + r;
+    const uint16_t* brow = nullptr;                    // this row of the bias
+    if constexpr (BIAS) brow = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, q);
     bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 27));
     const float* LD = reinterpret_cast<const float*>(smem + L::OFF_LD);
     const float nlq = ok ? LD[r] : 0.f;                // -L*log2(e) of this query row
@@ -269,11 +271,30 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32], pk[16];
         tmem_ld_x32(tS + 32 * ch, sr);
+        float bv[32];                                  // bias of (query q, keys of this chunk)
+        if constexpr (BIAS) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float v8[8];
+            if (q < sq.nq) {
+              bias8<BF16>(brow, kv0 + 64 * grp + 32 * ch + 8 * j, sq.nk, v8);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v8[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bv[8 * j + e] = v8[e];
+          }
+        }
         tmem_ld_wait();
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
           const int c = 32 * ch + 2 * c2;
-          const float2 x = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1])), sc2, nl2));
+          float2 x = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1])), sc2, nl2));
+          if constexpr (BIAS) {
+            x.x = fmaf(bv[2 * c2], 1.4426950408889634f, x.x);
+            x.y = fmaf(bv[2 * c2 + 1], 1.4426950408889634f, x.y);
+          }
           float p0 = ex2_approx(x.x);
           float p1 = ex2_approx(x.y);
           if (need_mask) {
@@ -332,11 +353,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool BIAS>
 cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                      const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   using L = Layout<D>;
-  auto kern = bwd_dq_kernel<D, BF16>;
+  auto kern = bwd_dq_kernel<D, BF16, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   Params p;
@@ -358,9 +379,19 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
 
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  if (a.pb.d > 64)
-    return a.pb.bf16 ? launch_t<128, true>(a, tq, tdo, tk, tv, stream) : launch_t<128, false>(a, tq, tdo, tk, tv, stream);
-  return a.pb.bf16 ? launch_t<64, true>(a, tq, tdo, tk, tv, stream) : launch_t<64, false>(a, tq, tdo, tk, tv, stream);
+  const bool bias = a.pb.bias != nullptr;
+  if (a.pb.d > 64) {
+    if (a.pb.bf16)
+      return bias ? launch_t<128, true, true>(a, tq, tdo, tk, tv, stream)
+                  : launch_t<128, true, false>(a, tq, tdo, tk, tv, stream);
+    return bias ? launch_t<128, false, true>(a, tq, tdo, tk, tv, stream)
+                : launch_t<128, false, false>(a, tq, tdo, tk, tv, stream);
+  }
+  if (a.pb.bf16)
+    return bias ? launch_t<64, true, true>(a, tq, tdo, tk, tv, stream)
+                : launch_t<64, true, false>(a, tq, tdo, tk, tv, stream);
+  return bias ? launch_t<64, false, true>(a, tq, tdo, tk, tv, stream)
+              : launch_t<64, false, false>(a, tq, tdo, tk, tv, stream);
 }
 
 }  // namespace fa

@@ -54,8 +54,8 @@
 namespace fa {
 namespace {
 
-constexpr int BN = 128;       // KV rows per CTA (TMEM lanes)
-constexpr int BM = 64;        // query rows per tile
+constexpr int BN = kMainBN;   // KV rows per CTA (TMEM lanes)
+constexpr int BM = kMainBM;   // query rows per tile
 constexpr int STAGES = 4;     // Q/dO ring depth: loads run ~2 tiles ahead of use
 constexpr int kThreads = 512;
 
@@ -131,7 +131,7 @@ __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&pk)[
     if (8 * i < cols) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
-template <int D, bool BF16, bool DET>
+template <int D, bool BF16, bool DET, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -355,9 +355,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* ds_row = smem + L::OFF_DS + r * 128;
     const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
     int qi = i0;                                          // query tile of tile t (walked, no division)
-    for (int t = 0; t < T; ++t, qi = (qi + 1 == nQt) ? i0 : qi + 1) {
+    int h = hkv * G;                                      // and its query head
+    for (int t = 0; t < T; ++t, h += (qi + 1 == nQt), qi = (qi + 1 == nQt) ? i0 : qi + 1) {
       const int s = t & (STAGES - 1);
       const int q0 = qi * BM;
+      const int qc = q0 + 32 * grp;                       // query of this group's column 0
+      float bv[32];                                       // bias of (query qc + c, key kv)
+      if constexpr (BIAS) {
+        const uint16_t* bcol = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, qc) + kv;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          bv[c] = (row_ok && qc + c < sq.nq) ? half_to_float<BF16>(__ldg(bcol + c * p.m.bias_st.n)) : 0.f;
+      }
       const float* Ls = reinterpret_cast<const float*>(smem + L::OFF_LD + s * L::LD_BYTES) + 32 * grp;
       const float* Ds = Ls + BM;
       const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BM + 32 * grp;
@@ -378,8 +387,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // x = S * scale * log2(e) + (-L * log2(e)), two columns per instruction
           const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(Ls + 4 * c4);
           const int c = 4 * c4;
-          const float2 xa = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 0]), __uint_as_float(sr[4 * c4 + 1])), sc2, nl.x));
-          const float2 xb = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])), sc2, nl.y));
+          float2 xa = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 0]), __uint_as_float(sr[4 * c4 + 1])), sc2, nl.x));
+          float2 xb = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])), sc2, nl.y));
+          if constexpr (BIAS) {
+            xa.x = fmaf(bv[c + 0], 1.4426950408889634f, xa.x);
+            xa.y = fmaf(bv[c + 1], 1.4426950408889634f, xa.y);
+            xb.x = fmaf(bv[c + 2], 1.4426950408889634f, xb.x);
+            xb.y = fmaf(bv[c + 3], 1.4426950408889634f, xb.y);
+          }
           float e0 = ex2_approx(xa.x);
           float e1 = ex2_approx(xa.y);
           float e2 = ex2_approx(xb.x);
@@ -421,6 +436,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               sub_f32x2(f2_bits(__uint_as_float(dr[4 * c4 + 2]), __uint_as_float(dr[4 * c4 + 3])), d2.y)));
           dk[2 * c4] = pack2<BF16>(sa.x, sa.y);
           dk[2 * c4 + 1] = pack2<BF16>(sbv.x, sbv.y);
+        }
+      }
+      if constexpr (BIAS) {
+        // dBias = dS (the bias enters S with weight 1), the 16-bit values G4 and G5 use
+        if (p.m.dbias != nullptr && row_ok) {
+          uint16_t* dcol = static_cast<uint16_t*>(p.m.dbias) + bias_row(p.m.dbias_st, b, h, qc) + kv;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (qc + c < sq.nq) dcol[c * p.m.dbias_st.n] = static_cast<uint16_t>(dk[c >> 1] >> (16 * (c & 1)));
         }
       }
       {
@@ -517,11 +541,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
-template <int D, bool BF16, bool DET>
+template <int D, bool BF16, bool DET, bool BIAS>
 cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                      const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   using L = Layout<D>;
-  auto kern = bwd_main_kernel<D, BF16, DET>;
+  auto kern = bwd_main_kernel<D, BF16, DET, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   Params p;
@@ -542,21 +566,28 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   return cudaGetLastError();
 }
 
+template <int D, bool BF16, bool DET>
+cudaError_t launch_b(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
+                     const CUtensorMap& tv, cudaStream_t stream) {
+  return a.pb.bias != nullptr ? launch_t<D, BF16, DET, true>(a, tq, tdo, tk, tv, stream)
+                              : launch_t<D, BF16, DET, false>(a, tq, tdo, tk, tv, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   const bool det = a.pb.deterministic != 0;
   if (a.pb.d > 64) {
-    if (a.pb.bf16) return det ? launch_t<128, true, true>(a, tq, tdo, tk, tv, stream)
-                              : launch_t<128, true, false>(a, tq, tdo, tk, tv, stream);
-    return det ? launch_t<128, false, true>(a, tq, tdo, tk, tv, stream)
-               : launch_t<128, false, false>(a, tq, tdo, tk, tv, stream);
+    if (a.pb.bf16) return det ? launch_b<128, true, true>(a, tq, tdo, tk, tv, stream)
+                              : launch_b<128, true, false>(a, tq, tdo, tk, tv, stream);
+    return det ? launch_b<128, false, true>(a, tq, tdo, tk, tv, stream)
+               : launch_b<128, false, false>(a, tq, tdo, tk, tv, stream);
   }
-  if (a.pb.bf16) return det ? launch_t<64, true, true>(a, tq, tdo, tk, tv, stream)
-                            : launch_t<64, true, false>(a, tq, tdo, tk, tv, stream);
-  return det ? launch_t<64, false, true>(a, tq, tdo, tk, tv, stream)
-             : launch_t<64, false, false>(a, tq, tdo, tk, tv, stream);
+  if (a.pb.bf16) return det ? launch_b<64, true, true>(a, tq, tdo, tk, tv, stream)
+                            : launch_b<64, true, false>(a, tq, tdo, tk, tv, stream);
+  return det ? launch_b<64, false, true>(a, tq, tdo, tk, tv, stream)
+             : launch_b<64, false, false>(a, tq, tdo, tk, tv, stream);
 }
 
 }  // namespace fa

@@ -78,7 +78,7 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -216,7 +216,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + lane_off + L::COL_O;
     const int q = q0 + r;
-    float m_ref = 0.f;                                  // reference max (log2 units)
+    const uint16_t* brow = nullptr;                     // this row of the bias
+    if constexpr (BIAS) brow = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, q);
+    float m_ref = -CUDART_INF_F;                        // reference max (log2 units); -inf: no key seen yet
     float l = 0.f;                                      // sum of 2^(x - m_ref)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -233,9 +235,30 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int ch = 0; ch < BK / 32; ++ch) {
         uint32_t sr[32];
         tmem_ld_x32(tS + 32 * ch, sr);
-        tmem_ld_wait();
+        if constexpr (BIAS) {
+          // x = S * scale * log2(e) + bias * log2(e)
+          float bv[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[32 * ch + c] = __uint_as_float(sr[c]) * p.scale_log2;
+          for (int j = 0; j < 4; ++j) {
+            float v8[8];
+            if (q < sq.nq) {
+              bias8<BF16>(brow, kv0 + 32 * ch + 8 * j, sq.nk, v8);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v8[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bv[8 * j + e] = v8[e];
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            x[32 * ch + c] = fmaf(bv[c], 1.4426950408889634f, __uint_as_float(sr[c]) * p.scale_log2);
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[32 * ch + c] = __uint_as_float(sr[c]) * p.scale_log2;
+        }
       }
       float mt = -CUDART_INF_F;
 #pragma unroll
@@ -243,12 +266,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (need_mask && c >= lim) x[c] = -CUDART_INF_F;
         mt = fmaxf(mt, x[c]);
       }
-      if (t == 0) {
-        m_ref = (mt == -CUDART_INF_F) ? 0.f : mt;
-      } else {
-        // Move the reference max only when P would exceed 2^8; then O and the sum are
+      {
+        // The first visible key sets the reference max (O and the sum are still 0).
+        // After that it moves only when P would exceed 2^8; then O and the sum are
         // rescaled, which needs the previous P V to have completed.
-        const bool resc = mt > m_ref + kRescaleThreshold;
+        const bool first = m_ref == -CUDART_INF_F;
+        const bool resc = !first && mt > m_ref + kRescaleThreshold;
+        if (first) m_ref = mt;
         if (__any_sync(0xffffffffu, resc)) {
           if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV), (t - 1) & 1, wc, 57))) { ok = false; break; }
           tc_fence_after();
@@ -269,14 +293,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           }
         }
       }
+      const float m_use = m_ref == -CUDART_INF_F ? 0.f : m_ref;   // no key yet: every x is -inf
       float lsum = 0.f;
 #pragma unroll
       for (int ch = 0; ch < BK / 32; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
-          const float p0 = ex2_approx(x[32 * ch + 2 * c2] - m_ref);
-          const float p1 = ex2_approx(x[32 * ch + 2 * c2 + 1] - m_ref);
+          const float p0 = ex2_approx(x[32 * ch + 2 * c2] - m_use);
+          const float p1 = ex2_approx(x[32 * ch + 2 * c2 + 1] - m_use);
           lsum += p0 + p1;
           pk[c2] = pack2<BF16>(p0, p1);
         }
@@ -331,11 +356,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool BIAS>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      unsigned int* status, cudaStream_t stream) {
   using L = Layout<D>;
-  auto kern = fwd_kernel<D, BF16>;
+  auto kern = fwd_kernel<D, BF16, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   Params p;
@@ -355,11 +380,19 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        unsigned int* status, cudaStream_t stream) {
-  if (a.pb.d > 64)
-    return a.pb.bf16 ? launch_t<128, true>(a, tq, tk, tv, status, stream)
-                     : launch_t<128, false>(a, tq, tk, tv, status, stream);
-  return a.pb.bf16 ? launch_t<64, true>(a, tq, tk, tv, status, stream)
-                   : launch_t<64, false>(a, tq, tk, tv, status, stream);
+  const bool bias = a.pb.bias != nullptr;
+  if (a.pb.d > 64) {
+    if (a.pb.bf16)
+      return bias ? launch_t<128, true, true>(a, tq, tk, tv, status, stream)
+                  : launch_t<128, true, false>(a, tq, tk, tv, status, stream);
+    return bias ? launch_t<128, false, true>(a, tq, tk, tv, status, stream)
+                : launch_t<128, false, false>(a, tq, tk, tv, status, stream);
+  }
+  if (a.pb.bf16)
+    return bias ? launch_t<64, true, true>(a, tq, tk, tv, status, stream)
+                : launch_t<64, true, false>(a, tq, tk, tv, status, stream);
+  return bias ? launch_t<64, false, true>(a, tq, tk, tv, status, stream)
+              : launch_t<64, false, false>(a, tq, tk, tv, status, stream);
 }
 
 }  // namespace fa

@@ -12,6 +12,11 @@ namespace fa {
 // Rows of every per-head query array in the workspace are padded to this.
 constexpr int kRowPad = 128;
 
+// Tile of the main backward kernel: KV rows per CTA and query rows per step.
+// The dBias zeroing kernel reproduces which (query tile, KV tile) pairs it skips.
+constexpr int kMainBN = 128;
+constexpr int kMainBM = 64;
+
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Workspace carve-up shared by every stage of the backward.
@@ -41,6 +46,12 @@ struct SeqMap {
   int total_q, total_k;  // packed: rows per head
   int causal_mode;   // 0 none, 1 top-left, 2 bottom-right
   Strides st;
+  // Additive bias [B, Hq, Nq, Nkv] in the 16-bit dtype (key axis contiguous,
+  // indices local to the sequence) and its gradient, or nullptr.
+  const void* bias;
+  Str3 bias_st;      // element strides of the batch, head and query axes (0 broadcasts)
+  void* dbias;
+  Str3 dbias_st;
 };
 
 struct Problem {
@@ -55,6 +66,10 @@ struct Problem {
   const int* cu_k;
   int total_q, total_k;
   Strides st;
+  const void* bias;
+  Str3 bias_st;
+  void* dbias;
+  Str3 dbias_st;
 };
 
 inline SeqMap seq_map(const Problem& pb) {
@@ -67,6 +82,10 @@ inline SeqMap seq_map(const Problem& pb) {
   m.total_q = pb.total_q; m.total_k = pb.total_k;
   m.causal_mode = pb.causal_mode;
   m.st = pb.st;
+  m.bias = pb.bias;
+  m.bias_st = pb.bias_st;
+  m.dbias = pb.dbias;
+  m.dbias_st = pb.dbias_st;
   return m;
 }
 
@@ -100,6 +119,8 @@ cudaError_t launch_preprocess(const Problem& pb, const void* o, const void* dO, 
 cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, unsigned int* status,
                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cudaStream_t stream);
+// Writes dBias = 0 where the main kernel, under causal tile skipping, never visits.
+cudaError_t launch_dbias_zero(const Problem& pb, unsigned int* status, cudaStream_t stream);
 
 // bwd_main.cu: maps are Q, dO (box 64 x 64 rows), K, V (box 64 x 128 rows)
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,

@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -65,6 +66,37 @@ __device__ __forceinline__ int bcoord(const SeqMap& m, int b) { return m.cu_q ? 
 // (row already includes the sequence's first row).
 __device__ __forceinline__ long long at(const Str3& s, const SeqMap& m, int b, int h, long long row) {
   return static_cast<long long>(bcoord(m, b)) * s.b + static_cast<long long>(h) * s.h + row * s.n;
+}
+
+// Element offset of query row q (local to its sequence) of head h of sequence b
+// in the bias or dBias tensor with strides s (the key index is added by the caller).
+__device__ __forceinline__ long long bias_row(const Str3& s, int b, int h, int q) {
+  return static_cast<long long>(b) * s.b + static_cast<long long>(h) * s.h + static_cast<long long>(q) * s.n;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float half_to_float(uint16_t u) {
+  if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(u) << 16);
+  else return __half2float(__ushort_as_half(u));
+}
+
+// Bias of keys col .. col + 7 of one row (16-byte aligned when col is a multiple
+// of 8); keys at or past nk read as 0 without touching memory.
+template <bool BF16>
+__device__ __forceinline__ void bias8(const uint16_t* row, int col, int nk, float (&v)[8]) {
+  if (col + 8 <= nk) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + col));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack2<BF16>(w[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = col + e < nk ? half_to_float<BF16>(__ldg(row + col + e)) : 0.f;
+  }
 }
 
 }  // namespace fa

@@ -184,3 +184,44 @@ def backward_strided(q, k, v, o, do, lse, scale: float, causal, deterministic: b
     _check(_lib.fa_bwd_strided(q, k, v, o, do, lse, dq, dk, dv, st, None, None, B, Hq, Hkv, Nq, Nkv, 0, 0, d, scale,
                                causal, _DT[q.dtype], int(deterministic), ws, n, s), "fa_bwd_strided")
     return dq, dk, dv
+
+
+# ------------------------------------------------------------ additive bias
+
+def _bias_strides(bias):
+    """(b, h, q) element strides of a [B or 1, Hq or 1, Nq, Nkv] bias; size-1 axes broadcast (stride 0)."""
+    if bias.dim() != 4 or bias.stride(-1) != 1:
+        raise ValueError("bias must be a 4-D tensor with a contiguous key axis")
+    st = bias.stride()
+    return (0 if bias.shape[0] == 1 else st[0], 0 if bias.shape[1] == 1 else st[1],
+            0 if bias.shape[2] == 1 else st[2])
+
+
+def forward_bias(q, k, v, bias, scale: float, causal, stream=None):
+    """Forward with an additive bias [B or 1, Hq or 1, Nq, Nkv] (same dtype as q; -inf masks a key)."""
+    _need(q, k, v)
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    fb = _lib.make_bias(bias, _bias_strides(bias))
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_fwd_bias(q, k, v, o, lse, fb, None, None, None, B, Hq, Hkv, Nq, Nkv, 0, 0, d, scale, causal,
+                            _DT[q.dtype], s), "fa_fwd_bias")
+    return o, lse
+
+
+def backward_bias(q, k, v, o, do, lse, bias, scale: float, causal, deterministic: bool = False, want_dbias=True,
+                  stream=None):
+    """Backward with an additive bias.  Returns (dQ, dK, dV, dBias); dBias [B, Hq, Nq, Nkv] is dS of every
+    head (None unless ``want_dbias``); sum it over the axes the bias broadcasts."""
+    _need(q, k, v, o, do, lse)
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbias = torch.empty(B, Hq, Nq, Nkv, dtype=q.dtype, device=q.device) if want_dbias else None
+    fb = _lib.make_bias(bias, _bias_strides(bias), dbias, dbias.stride()[:3] if dbias is not None else (0, 0, 0))
+    n = _lib.fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, int(deterministic))
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(_lib.fa_bwd_bias(q, k, v, o, do, lse, dq, dk, dv, fb, None, None, None, B, Hq, Hkv, Nq, Nkv, 0, 0, d,
+                            scale, causal, _DT[q.dtype], int(deterministic), ws, n, s), "fa_bwd_bias")
+    return dq, dk, dv, dbias

@@ -270,6 +270,49 @@ int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, c
                    float scale, int causal, int dtype, int deterministic,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Additive attention bias.  "[Kernel] Flash attention 2" (Liger-Kernel #275,
+ * "Details") supports attention bias and attention masking: the bias is added
+ * to the scaled scores before the causal mask,
+ *   S = scale * Q K^T + bias,
+ * and a boolean mask is the bias -inf at the dropped keys (a row that keeps no
+ * key gets O = 0, L = -inf).  The bias enters S with weight 1, so its gradient
+ * is dBias = dS = P o (dP - D) of every query head.
+ * bias: 16-bit (the dtype of Q), a [B, Hq, Nq, Nkv] view with the key axis
+ *   contiguous and element strides bias_strides.b / .h / .n for the batch,
+ *   head and query axes; a stride of 0 broadcasts that axis.  Indices are local
+ *   to the sequence for packed batches.  Base 16-byte aligned, strides
+ *   multiples of 8.
+ * dbias (fa_bwd_bias only, may be NULL): 16-bit output [B, Hq, Nq, Nkv] with
+ *   positive strides (every row its own), fully overwritten for every query
+ *   and key of every sequence (0 where the causal mask drops the key).  A
+ *   caller whose bias broadcasts sums dbias over the broadcast axes.
+ */
+typedef struct {
+  const void* bias;
+  fa_stride3 bias_strides;
+  void* dbias;
+  fa_stride3 dbias_strides;
+} fa_bias;
+
+/*
+ * fa_fwd_bias / fa_bwd_bias -- fa_fwd_strided / fa_bwd_strided with an additive
+ * bias (bias == NULL: none; fa_fwd_bias takes no dbias).
+ */
+int fa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse,
+                const fa_bias* bias, const fa_strides* strides,
+                const int* cu_seqlens_q, const int* cu_seqlens_k,
+                int B, int Hq, int Hkv, int Nq, int Nkv, int total_q, int total_k, int d,
+                float scale, int causal, int dtype, cudaStream_t stream);
+
+int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv,
+                const fa_bias* bias, const fa_strides* strides,
+                const int* cu_seqlens_q, const int* cu_seqlens_k,
+                int B, int Hq, int Hkv, int Nq, int Nkv, int total_q, int total_k, int d,
+                float scale, int causal, int dtype, int deterministic,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of an fa_status value (static string, never NULL). */
 const char* fa_strerror(int status);
 

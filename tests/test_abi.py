@@ -192,3 +192,26 @@ def test_bwd_strided_validates_strides(lib, over, code):
 def test_strided_offsets_must_come_in_pairs(lib):
     r = _lib.fa_fwd_strided(A, A, A, A, A, None, None, C, 1, 2, 1, 16, 16, 16, 16, 64, 0.1, 0, _lib.FA_BF16)
     assert r == _lib.FA_ERR_NULL
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bias=None, bs=(0, 0, 64)), _lib.FA_ERR_NULL),               # description without a bias
+    (dict(bias=A + 8), _lib.FA_ERR_ALIGN),
+    (dict(bs=(0, 0, 60)), _lib.FA_ERR_ARG),                          # query stride not a multiple of 8
+    (dict(bs=(-8, 0, 64)), _lib.FA_ERR_ARG),
+    (dict(dbias=A, dbs=(0, 4096, 64)), _lib.FA_ERR_ARG),             # dBias rows must not broadcast
+    (dict(dbias=A + 4, dbs=(8192, 4096, 64)), _lib.FA_ERR_ALIGN),
+])
+def test_bwd_bias_validates(lib, kw, code):
+    args = dict(bias=A, bs=(0, 0, 64), dbias=None, dbs=(0, 0, 0))
+    args.update(kw)
+    fb = _lib.make_bias(args["bias"], args["bs"], args["dbias"], args["dbs"])
+    r = _lib.fa_bwd_bias(A, A, A, A, A, A, A, A, A, fb, None, None, None, 1, 2, 1, 64, 64, 0, 0, 64, 0.1, 1,
+                         _lib.FA_BF16, 0, W, 1 << 30)
+    assert r == code
+
+
+def test_fwd_bias_takes_no_dbias(lib):
+    fb = _lib.make_bias(A, (0, 0, 64), A, (8192, 4096, 64))
+    assert _lib.fa_fwd_bias(A, A, A, A, A, fb, None, None, None, 1, 2, 1, 64, 64, 0, 0, 64, 0.1, 0,
+                            _lib.FA_BF16) == _lib.FA_ERR_ARG
