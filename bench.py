@@ -10,6 +10,13 @@ forward, outside the timed region.  Every input is larger than L2.
 Metric: backward TFLOP/s counting 10*B*Hq*Nq*Nkv*d FLOPs, halved for causal.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--deterministic]
+    python bench.py --feature {varlen,bias,bshd} [--steps K] [--warmup W]
+
+--feature times one of the widened paths on its own workload (one JSON line,
+same metric; not part of the headline):
+  varlen  packed batch of 16 Llama-3 shaped sequences, seeded lengths 512..8192, causal
+  bias    the headline shape at N=4096 with a per-head bias [1, 32, N, N] and dBias
+  bshd    the headline workload with every tensor stored [B, N, H, d] (strided)
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (the
 problem shards by (batch, kv-head) groups with no exchange): weak scaling,
@@ -43,6 +50,7 @@ def parse():
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--n", type=int, default=8192, help="sequence length of the Llama-3 shaped workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--feature", choices=["varlen", "bias", "bshd"], default=None)
     return ap.parse_args()
 
 
@@ -206,10 +214,72 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def run_feature(args):
+    """Times one widened path (packed batch, bias with dBias, strided storage) on its workload."""
+    import random
+
+    import torch
+    from attn_bwd_gb300 import _lib, inputs, torch_api
+
+    torch.cuda.set_device(0)
+    _lib.load()
+    det = args.deterministic
+    if args.feature == "varlen":
+        rnd = random.Random(7)
+        lens = [rnd.randrange(512, 8193, 64) for _ in range(16)]
+        pk = inputs.Packed(tuple(lens), tuple(lens), 32, 8, 128, 1, "bf16")
+        q, k, v, do = inputs.draw_packed(pk, 7, device="cuda")
+        o, lse = torch_api.forward_varlen(q, k, v, pk.cu_q, pk.cu_k, pk.softmax_scale, 1)
+        fl = sum(10.0 * 32 * n * n * 128 / 2 for n in lens)
+        call = lambda: torch_api.backward_varlen(q, k, v, o, do, lse, pk.cu_q, pk.cu_k, pk.softmax_scale, 1, det)  # noqa: E731
+        desc = {"workload": f"packed batch of 16 causal sequences, lengths {min(lens)}..{max(lens)} "
+                            f"(total {sum(lens)} tokens), Hq=32 Hkv=8 d=128 bf16", "lengths": lens}
+    elif args.feature == "bias":
+        n = 4096
+        sh = inputs.Shape(4, 32, 8, n, n, 128, True, "bf16")
+        q, k, v, do = inputs.draw(sh, 8, device="cuda")
+        g = torch.Generator(device="cuda").manual_seed(9)
+        bias = torch.randn(1, 32, n, n, generator=g, device="cuda").to(torch.bfloat16)
+        o, lse = torch_api.forward_bias(q, k, v, bias, sh.softmax_scale, True)
+        fl = flops(sh)
+        call = lambda: torch_api.backward_bias(q, k, v, o, do, lse, bias, sh.softmax_scale, True, det)  # noqa: E731
+        desc = {"workload": f"B=4 Hq=32 Hkv=8 N={n} d=128 bf16 causal, bias [1, 32, N, N], dBias [4, 32, N, N]"}
+    else:
+        sh = workload(args.n)
+        q, k, v, do = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in inputs.draw(sh, 10, device="cuda"))
+        o, lse = torch_api.forward_strided(q, k, v, sh.softmax_scale, True)
+        fl = flops(sh)
+        call = lambda: torch_api.backward_strided(q, k, v, o, do, lse, sh.softmax_scale, True, det)  # noqa: E731
+        desc = {"workload": "headline workload stored [B, N, H, d] (strided views)"}
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    if _lib.fa_last_device_error() != 0:
+        raise RuntimeError("device status reported a failure")
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks, _ = load_peaks()
+    tf = fl / (ms * 1e-3) / 1e12
+    print(json.dumps({"metric": METRIC, "feature": args.feature, "value": tf, "unit": "TFLOP/s", "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                      "dtype": "bf16", "data": "synthetic", "deterministic": det,
+                      "frac_of_measured_bf16_peak": tf / float(peaks["bf16_tflops"]),
+                      "note": "whole backward through the torch front end (workspace and outputs allocated per call)",
+                      "config": desc}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         reference_arm(args)
+        return
+    if args.feature:
+        run_feature(args)
         return
     import torch
     import torch.distributed as dist
