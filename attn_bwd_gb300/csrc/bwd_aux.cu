@@ -142,30 +142,29 @@ __global__ void wait_selftest_kernel(unsigned int* status, long long timeout_ns)
 // Query row q (tile qt = q / BM) is skipped exactly for the KV tiles j with
 // i0(j) > qt, i.e. j*BN >= (qt + 1)*BM + delta: keys from
 // jmin*BN = ceil(((qt + 1)*BM + delta) / BN) * BN to the end of the row.
-// One thread writes 8 keys (16 bytes) of one row.
+// One warp per row, 16 bytes per lane and store.
 template <bool BF16>
 __global__ void __launch_bounds__(256)
-dbias_zero_kernel(SeqMap m, long long rows, int kchunks, unsigned int* status) {
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < rows * kchunks;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = idx / kchunks;                  // (b, h, q) with q < Nq (the longest length)
-    const int c8 = static_cast<int>(idx - row * kchunks);
-    const int q = static_cast<int>(row % m.Nq);
-    const long long bh = row / m.Nq;
+dbias_zero_kernel(SeqMap m, long long rows, unsigned int* status) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows;
+       row += nwarps) {
+    const long long bh = row / m.Nq;                       // rows are (b, h, q) with q < Nq (the longest)
+    const int q = static_cast<int>(row - bh * m.Nq);
     const int b = static_cast<int>(bh / m.Hq);
     const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
     const Seq sq = seq_of(m, b, status, 32);
     if (q >= sq.nq) continue;
     const long long first = static_cast<long long>(q / kMainBM + 1) * kMainBM + sq.delta;
-    const long long jmin = first <= 0 ? 0 : (first + kMainBN - 1) / kMainBN;
-    const long long kv = 8LL * c8;
-    if (kv + 8 <= jmin * kMainBN || kv >= sq.nk) continue;
+    const long long k0 = (first <= 0 ? 0 : (first + kMainBN - 1) / kMainBN) * kMainBN;
     uint16_t* dst = static_cast<uint16_t*>(m.dbias) + bias_row(m.dbias_st, b, h, q);
-    if (kv >= jmin * kMainBN && kv + 8 <= sq.nk) {
-      *reinterpret_cast<uint4*>(dst + kv) = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-      for (long long e = kv; e < kv + 8 && e < sq.nk; ++e)
-        if (e >= jmin * kMainBN) dst[e] = 0;
+    for (long long kv = k0 + 8 * lane; kv < sq.nk; kv += 256) {
+      if (kv + 8 <= sq.nk) {
+        *reinterpret_cast<uint4*>(dst + kv) = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        for (long long e = kv; e < sq.nk; ++e) dst[e] = 0;
+      }
     }
   }
 }
@@ -218,12 +217,11 @@ cudaError_t launch_dq_convert(const Problem& pb, const Workspace& ws, void* dq, 
 
 cudaError_t launch_dbias_zero(const Problem& pb, unsigned int* status, cudaStream_t stream) {
   const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.Nq;
-  const int kchunks = (pb.Nkv + 7) / 8;
-  const long long grid = grid_for(rows * kchunks, 256);
+  const long long grid = grid_for(rows, 8);                 // 8 rows (warps) per block
   if (pb.bf16)
-    dbias_zero_kernel<true><<<static_cast<unsigned>(grid), 256, 0, stream>>>(seq_map(pb), rows, kchunks, status);
+    dbias_zero_kernel<true><<<static_cast<unsigned>(grid), 256, 0, stream>>>(seq_map(pb), rows, status);
   else
-    dbias_zero_kernel<false><<<static_cast<unsigned>(grid), 256, 0, stream>>>(seq_map(pb), rows, kchunks, status);
+    dbias_zero_kernel<false><<<static_cast<unsigned>(grid), 256, 0, stream>>>(seq_map(pb), rows, status);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,7 @@ constexpr int BN = kMainBN;   // KV rows per CTA (TMEM lanes)
 constexpr int BM = kMainBM;   // query rows per tile
 constexpr int STAGES = 4;     // Q/dO ring depth: loads run ~2 tiles ahead of use
 constexpr int kThreads = 512;
+constexpr int kGroupChunk = 32;   // (batch, kv-head) groups per launch-order chunk
 
 template <int D>
 struct Layout {
@@ -149,12 +150,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
-  // ---- work item: KV tile j of key/value head hkv of batch b, tile-major, so
-  // that under causal masking the longest CTAs (small j) are scheduled first.
-  // (A (batch, kv-head)-major order, tried for L2 reuse, measured slower.)
+  // ---- work item: KV tile j of key/value head hkv of batch b.  The (batch,
+  // kv-head) groups are taken in chunks of kGroupChunk, and inside a chunk the
+  // order is tile-major, so that under causal masking the longest CTAs (small j)
+  // start first and several KV tiles of each group run at the same time: they
+  // sweep the same query tiles together, so their dQ reductions meet in L2.
+  // (With more groups in flight than that, each group has about one CTA live
+  // and nearly every reduction misses L2; a fully group-major order measured
+  // slower on the dense headline, whose 32 groups fit one chunk.)
   const int groups = p.B * p.Hkv;
-  const int j = blockIdx.x / groups;
-  const int gi = blockIdx.x - j * groups;
+  const int nKt = (p.Nkv + BN - 1) / BN;
+  const int chunk = static_cast<int>(blockIdx.x) / (kGroupChunk * nKt);
+  const int rem = static_cast<int>(blockIdx.x) - chunk * (kGroupChunk * nKt);
+  const int cg = min(kGroupChunk, groups - chunk * kGroupChunk);   // groups in this chunk
+  const int j = rem / cg;
+  const int gi = chunk * kGroupChunk + (rem - j * cg);
   const int b = gi / p.Hkv;
   const int hkv = gi - b * p.Hkv;
   const int G = p.Hq / p.Hkv;

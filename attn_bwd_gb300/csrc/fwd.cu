@@ -219,6 +219,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint16_t* brow = nullptr;                     // this row of the bias
     if constexpr (BIAS) brow = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, q);
     float m_ref = -CUDART_INF_F;                        // reference max (log2 units); -inf: no key seen yet
+    const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
     float l = 0.f;                                      // sum of 2^(x - m_ref)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -257,15 +258,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         } else {
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) x[32 * ch + c] = __uint_as_float(sr[c]) * p.scale_log2;
+          for (int c2 = 0; c2 < 16; ++c2) {   // two columns per instruction
+            const float2 xx = f2_split(mul_f32x2(f2_bits(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1])),
+                                                 sc2));
+            x[32 * ch + 2 * c2] = xx.x;
+            x[32 * ch + 2 * c2 + 1] = xx.y;
+          }
         }
       }
-      float mt = -CUDART_INF_F;
+      // row max over eight independent partial maxima (a single running max is a
+      // 128-long dependency chain)
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = -CUDART_INF_F;
 #pragma unroll
       for (int c = 0; c < BK; ++c) {
         if (need_mask && c >= lim) x[c] = -CUDART_INF_F;
-        mt = fmaxf(mt, x[c]);
+        mp[c & 7] = fmaxf(mp[c & 7], x[c]);
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       {
         // The first visible key sets the reference max (O and the sum are still 0).
         // After that it moves only when P would exceed 2^8; then O and the sum are
@@ -294,21 +306,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
       }
       const float m_use = m_ref == -CUDART_INF_F ? 0.f : m_ref;   // no key yet: every x is -inf
-      float lsum = 0.f;
+      const uint64_t m2 = f2_bits(m_use, m_use);
+      float ls[8];                                         // partial row sums
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < BK / 32; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
-          const float p0 = ex2_approx(x[32 * ch + 2 * c2] - m_use);
-          const float p1 = ex2_approx(x[32 * ch + 2 * c2 + 1] - m_use);
-          lsum += p0 + p1;
+          const float2 xm = f2_split(sub_f32x2(f2_bits(x[32 * ch + 2 * c2], x[32 * ch + 2 * c2 + 1]), m2));
+          const float p0 = ex2_approx(xm.x);
+          const float p1 = ex2_approx(xm.y);
+          ls[c2 & 7] += p0 + p1;
           pk[c2] = pack2<BF16>(p0, p1);
         }
         // columns [16ch, 16ch+16) of S were already read
         tmem_st_x16(tS + 16 * ch, pk);
       }
-      l += lsum;
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
