@@ -33,7 +33,7 @@ namespace {
 
 constexpr int BQ = 128;     // query rows per CTA (TMEM lanes)
 constexpr int BK = 128;     // KV rows per step
-constexpr int STAGES = 2;   // K/V ring depth
+constexpr int STAGES = 3;   // K/V ring depth: a 64 KB load takes ~2 tile-times under load
 constexpr int kThreads = 256;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 
