@@ -35,7 +35,8 @@ namespace {
 
 constexpr int BQ = 128;    // query rows per CTA (TMEM lanes)
 constexpr int BK = 128;    // KV rows per step
-constexpr int STAGES = 2;  // K/V ring depth
+constexpr int KST = 3;     // K ring depth: K is held until dQ += dS K of its tile
+constexpr int VST = 2;     // V ring depth: V is free once dP = dO V^T of its tile completes
 constexpr int kThreads = 384;
 
 template <int D>
@@ -45,10 +46,11 @@ struct Layout {
   static constexpr int TILE = NH * HALF;        // one 128-row tile of Q, dO, K or V
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = TILE;
-  static constexpr int OFF_KV = 2 * TILE;       // stage s: K at OFF_KV + 2*s*TILE, V after it
-  static constexpr int OFF_LD = OFF_KV + STAGES * 2 * TILE;
+  static constexpr int OFF_K = 2 * TILE;        // K stage s at OFF_K + s*TILE
+  static constexpr int OFF_V = OFF_K + KST * TILE;   // V stage s at OFF_V + s*TILE
+  static constexpr int OFF_LD = OFF_V + VST * TILE;
   static constexpr int OFF_BAR = OFF_LD + 2 * BQ * 4;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = (TOTAL + 1024) > 120 * 1024 ? (TOTAL + 1024) : 120 * 1024;
@@ -60,10 +62,10 @@ struct Layout {
 };
 
 enum : int {
-  B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_DS = B_S + 2, B_SFREE = B_DS + 2,
-  B_DP = B_SFREE + 2, B_DPFREE, B_ACC, B_AFIN, B_END
+  B_Q = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST,
+  B_S = B_VEMPTY + VST, B_DS = B_S + 2, B_SFREE = B_DS + 2, B_DP = B_SFREE + 2, B_DPFREE, B_ACC, B_AFIN, B_END
 };
-static_assert(B_END <= 16, "barrier count");
+static_assert(B_END <= 24, "barrier count");
 
 struct Params {
   const float* nLg;
@@ -120,9 +122,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_KVFULL + s), 1);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(bar(B_S + j), 1);
@@ -158,24 +164,29 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
       bulk_load(sb + L::OFF_LD, p.nLg + row, BQ * 4, bar(B_Q));
       bulk_load(sb + L::OFF_LD + BQ * 4, p.Dv + row, BQ * 4, bar(B_Q));
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % STAGES;
-        const uint32_t ph = (t / STAGES) & 1;
-        if (t >= STAGES && !mbar_wait(bar(B_KVEMPTY + s), ph ^ 1, wc, 21)) break;
-        const uint32_t fb = bar(B_KVFULL + s);
-        mbar_arrive_expect_tx(fb, 2 * L::TILE);
-        const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
+        // K(t) once dQ(t - KST) has read its slot; V(t) once dP(t - VST) has read its slot
+        // (dP(t - 2) completes before dQ(t - 2), so the V wait never holds back K(t + 1))
+        const int ks = t % KST, vs = t % VST;
+        if (t >= KST && !mbar_wait(bar(B_KEMPTY + ks), ((t / KST) & 1) ^ 1, wc, 21)) break;
+        mbar_arrive_expect_tx(bar(B_KFULL + ks), L::TILE);
 #pragma unroll
-        for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_4d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
-          tma_load_4d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
-        }
-        issued = t + 1;
+        for (int hh = 0; hh < L::NH; ++hh)
+          tma_load_4d(sb + L::OFF_K + ks * L::TILE + hh * L::HALF, &tm_k, bar(B_KFULL + ks), 64 * hh,
+                      sq.k_start + t * BK, hk, bc);
+        k_issued = t + 1;
+        if (t >= VST && !mbar_wait(bar(B_VEMPTY + vs), ((t / VST) & 1) ^ 1, wc, 20)) break;
+        mbar_arrive_expect_tx(bar(B_VFULL + vs), L::TILE);
+#pragma unroll
+        for (int hh = 0; hh < L::NH; ++hh)
+          tma_load_4d(sb + L::OFF_V + vs * L::TILE + hh * L::HALF, &tm_v, bar(B_VFULL + vs), 64 * hh,
+                      sq.k_start + t * BK, hk, bc);
+        v_issued = t + 1;
       }
       drain_wait(bar(B_Q), 0);
-      for (int t = max(0, issued - STAGES); t < issued; ++t)
-        drain_wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1);
+      for (int t = max(0, k_issued - KST); t < k_issued; ++t) drain_wait(bar(B_KFULL + t % KST), (t / KST) & 1);
+      for (int t = max(0, v_issued - VST); t < v_issued; ++t) drain_wait(bar(B_VFULL + t % VST), (t / VST) & 1);
     }
   } else if (warp == 1 || warp == 2) {
     // ================================================================ MMA issuers
@@ -185,7 +196,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint32_t tdP = tmem + L::COL_DP, tdQ = tmem + L::COL_DQ;
       const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q, 16, 1024), dO_k = sw128_desc(sb + L::OFF_DO, 16, 1024);
       auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BK; };
-      auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_KV + (t % STAGES) * 2 * L::TILE; };
+      auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_K + (t % KST) * L::TILE; };
+      auto v_tile = [&](int t) -> uint32_t { return sb + L::OFF_V + (t % VST) * L::TILE; };
       // K-major step ks (16 elements of d): 64-column half ks/4, 32 bytes per step inside it
       auto kstep = [](int ks) -> uint64_t {
         return static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
@@ -196,21 +208,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (warp == 1) {
         bool ok = wait(bar(B_Q), 0, 22);
         for (int t = 0; ok && t < T; ++t) {
-          if (!wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1, 23)) break;
+          if (!wait(bar(B_KFULL + t % KST), (t / KST) & 1, 23)) break;
           if (t >= 2 && !wait(bar(B_SFREE + (t & 1)), ((t - 2) >> 1) & 1, 24)) break;
           tc_fence_after();
-          const uint32_t aK = k_tile(t);
-          const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aK + L::TILE, 16, 1024);
+          const uint64_t dK_k = sw128_desc(k_tile(t), 16, 1024), dV_k = sw128_desc(v_tile(t), 16, 1024);
           // G1: S = Q K^T into buffer t & 1
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) umma_ss_warp(s_buf(t), dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
           umma_commit_warp(bar(B_S + (t & 1)));
           // G2: dP = dO V^T, once the softmax groups have loaded dP of the previous tile
+          if (!wait(bar(B_VFULL + t % VST), (t / VST) & 1, 19)) break;
           if (t >= 1 && !wait(bar(B_DPFREE), (t - 1) & 1, 25)) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) umma_ss_warp(tdP, dO_k + kstep(ks), dV_k + kstep(ks), ID_S, ks > 0);
           umma_commit_warp(bar(B_DP));
+          umma_commit_warp(bar(B_VEMPTY + t % VST));     // V(t) is read by G2(t) only
         }
         umma_commit_warp(bar(B_AFIN));   // this warp's MMAs complete before TMEM is released
         drain_wait(bar(B_AFIN), 0);
@@ -226,8 +239,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             umma_ts_warp(tdQ, s_buf(t) + 64 * (ks >> 2) + 8 * (ks & 3),
                          dK_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_Q, (t > 0 || ks > 0));
           umma_commit_warp(bar(B_SFREE + (t & 1)));
-          // stage of tile t: G1/G2(t) have completed (dS(t) depends on them); G5(t) is tracked here
-          umma_commit_warp(bar(B_KVEMPTY + t % STAGES));
+          // K(t): G1(t) has completed (dS(t) depends on it); G5(t) is tracked here
+          umma_commit_warp(bar(B_KEMPTY + t % KST));
         }
         umma_commit_warp(bar(B_ACC));
         if (*abort_flag) drain_wait(bar(B_ACC), 0);
