@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libattn_bwd_gb300.so")
-SOURCES = ["api.cu", "bwd_main.cu", "bwd_dq.cu", "bwd_aux.cu", "fwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "bwd_main.cu", "bwd_dq.cu", "bwd_aux.cu", "fwd.cu", "noalloc.cu", "host_pipeline.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", "seq.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]

@@ -313,6 +313,30 @@ int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, cons
                 float scale, int causal, int dtype, int deterministic,
                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * fa_bwd_host -- fa_bwd for tensors in HOST memory (same layouts, contiguous),
+ * with the transfers overlapped with the computation.  The pages have no
+ * counterpart; it serves callers whose activations live in host memory (for
+ * example offloaded between the forward and the backward).  The batch is cut
+ * into chunks of chunk_b sequences that flow through two slots of the caller's
+ * DEVICE staging memory: while a chunk computes on `stream`, the next one is
+ * copied in and the previous one copied out on two copy streams the library
+ * creates once per device.  The call returns once everything is queued; the
+ * work is complete, dq/dk/dv written in host memory, when `stream` reaches
+ * this point.  Host buffers should be page-locked (cudaHostAlloc /
+ * cudaHostRegister); pageable memory works but serialises the copies.
+ * staging: >= fa_bwd_host_staging_size(...) bytes, 256-byte aligned, not used
+ * by anything else until `stream` passes the call.  chunk_b in [1, B].
+ */
+size_t fa_bwd_host_staging_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int deterministic,
+                                int chunk_b);
+
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv,
+                int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
+                int dtype, int deterministic, int chunk_b, void* staging, size_t staging_bytes,
+                cudaStream_t stream);
+
 /* Human-readable name of an fa_status value (static string, never NULL). */
 const char* fa_strerror(int status);
 

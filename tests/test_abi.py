@@ -215,3 +215,18 @@ def test_fwd_bias_takes_no_dbias(lib):
     fb = _lib.make_bias(A, (0, 0, 64), A, (8192, 4096, 64))
     assert _lib.fa_fwd_bias(A, A, A, A, A, fb, None, None, None, 1, 2, 1, 64, 64, 0, 0, 64, 0.1, 0,
                             _lib.FA_BF16) == _lib.FA_ERR_ARG
+
+
+def test_host_pipeline_validation_and_staging_size(lib):
+    one = _lib.fa_bwd_workspace_size(2, 4, 2, 100, 100, 64, 0)
+    assert one > 0
+    two_slots = _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 2)
+    one_slot = _lib.fa_bwd_host_staging_size(2, 4, 2, 100, 100, 64, 0, 2)
+    assert two_slots == 2 * one_slot and one_slot > one
+    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 0) == 0
+    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 6) == 0
+    args = [A] * 9 + [5, 4, 2, 100, 100, 64, 0.1, 1, _lib.FA_BF16, 0]
+    assert _lib.fa_bwd_host(*args, 0, W, 1 << 30) == _lib.FA_ERR_SHAPE
+    assert _lib.fa_bwd_host(*args, 2, None, 1 << 30) == _lib.FA_ERR_WORKSPACE
+    assert _lib.fa_bwd_host(*args, 2, W, 100) == _lib.FA_ERR_WORKSPACE
+    assert _lib.fa_bwd_host(*args, 2, W + 16, 1 << 30) == _lib.FA_ERR_ALIGN
