@@ -12,7 +12,8 @@
 // and dQ = scale * dQ is written once in the 16-bit dtype.
 //
 // Warp roles (384 threads):
-//   warp 0       TMA producer: Q, dO, -L*log2e, D once; K, V through a 2-stage ring
+//   warp 0       TMA producer: Q, dO, -L*log2e, D once; K through a 3-stage ring and
+//                V through a 2-stage ring (V is free after dP, K only after dQ)
 //   warp 1       owns TMEM; issues G1 and G2 (the products the softmax groups consume)
 //   warp 2       issues G5 (the product of what the softmax groups produce)
 //   warps 4-11   two softmax groups: thread r of group g owns query row r (TMEM

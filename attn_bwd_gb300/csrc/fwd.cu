@@ -16,7 +16,7 @@
 // more than 8, which keeps P <= 256 and makes rescaling rare after the first
 // tiles.
 //
-// Warp roles (256 threads): warp 0 TMA producer (Q once, K/V ring), warp 1 owns
+// Warp roles (256 threads): warp 0 TMA producer (Q once, 3-stage K/V ring), warp 1 owns
 // TMEM and issues G1, warp 2 issues PV, warps 4-7 thread r owns query row r
 // (TMEM lane r) and all 128 columns of each S tile.  S is double-buffered in
 // TMEM (S0, S1, O = 2 x 128 + d columns).

@@ -22,7 +22,7 @@ namespace fa {
 
 struct Seq {
   int nq, nk;            // queries and keys of this sequence
-  int q_start, k_start;  // first row of the sequence inside its slab
+  int q_start, k_start;  // first row of the sequence along its head's row axis
   int delta;             // causal: key j masked for query i when j > i + delta
 };
 

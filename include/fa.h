@@ -23,10 +23,13 @@
  * "Minimal Repro"), which accumulates dQ in an fp32 buffer across KV tiles;
  * GQA as listed in "[Kernel] Flash attention 2" (Liger-Kernel #275, "Details").
  *
- * Layout (all entry points): contiguous row-major tensors
+ * Layout: contiguous row-major tensors
  *   Q, O, dO, dQ : [B, Hq,  Nq,  d]   16-bit (fp16 or bf16, see fa_dtype)
  *   K, V, dK, dV : [B, Hkv, Nkv, d]   16-bit
  *   L (lse)      : [B, Hq,  Nq]       fp32, natural-log LSE of the scaled scores
+ * for every entry point except the packed-batch ones (fa_*_varlen: [H, total,
+ * d]), the strided ones (fa_*_strided, fa_*_bias: any batch, head and row
+ * strides) and fa_bwd_host (host memory).
  * d: a multiple of 8 from 8 to 128 ("[Kernel] Flash attention 2", "Details":
  * no restriction on the head dimension; 8 keeps every row a whole number of
  * 16-byte pieces, and 128 is the most whose dK and dV accumulators, 128 rows x
@@ -34,11 +37,12 @@
  * tiles).  Other sizes run on the d = 64 or d = 128 kernels, which read the
  * missing columns as zeros: exact, since a zero column adds nothing to Q K^T
  * and produces a zero column of O, dQ, dK, dV, which is not written.
- * Every pointer is a DEVICE pointer on the current
- * device, 16-byte aligned.  The caller owns every buffer (inputs, outputs and
- * workspace) and the stream; the library allocates no device memory, keeps no
- * state besides one status word per kernel family, and never synchronises
- * inside fa_fwd / fa_bwd*.  All work is enqueued on `stream`.
+ * Every pointer is a DEVICE pointer on the current device (except for
+ * fa_bwd_host), 16-byte aligned.  The caller owns every buffer (inputs,
+ * outputs, workspace, staging) and the stream; the library allocates no
+ * device memory, keeps no state besides one status word per kernel family
+ * (and fa_bwd_host's copy streams), and never synchronises inside fa_fwd* /
+ * fa_bwd*.  All work is enqueued on `stream`.
  *
  * Errors: each call validates its arguments first and, on failure, returns a
  * non-zero fa_status WITHOUT launching anything.  FA_ERR_CUDA reports a
