@@ -31,10 +31,11 @@
 namespace fa {
 namespace {
 
-constexpr int BQ = 128;     // query rows per CTA (TMEM lanes)
+constexpr int BQ = 128;     // query rows per tile (TMEM lanes)
+constexpr int NT = 2;       // query tiles per CTA, one softmax warpgroup each
 constexpr int BK = 128;     // KV rows per step
-constexpr int STAGES = 3;   // K/V ring depth: a 64 KB load takes ~2 tile-times under load
-constexpr int kThreads = 256;
+constexpr int STAGES = 2;   // K/V ring depth (each K/V tile serves both query tiles)
+constexpr int kThreads = 128 + NT * 128;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 
 template <int D>
@@ -42,22 +43,22 @@ struct Layout {
   static constexpr int NH = D / 64;
   static constexpr int HALF = 128 * 128;        // one 64-column half of a 128-row tile
   static constexpr int TILE = NH * HALF;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = TILE;           // stage s: K at OFF_KV + 2*s*TILE, V after it
+  static constexpr int OFF_Q = 0;               // query tile x at OFF_Q + x*TILE
+  static constexpr int OFF_KV = NT * TILE;      // stage s: K at OFF_KV + 2*s*TILE, V after it
   static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE;
   static constexpr int NBAR = 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = (TOTAL + 1024) > 120 * 1024 ? (TOTAL + 1024) : 120 * 1024;
-  static constexpr int COL_S = 0;               // buffers at 0 and BK
-  static constexpr int COL_O = 2 * BK;
-  static_assert(COL_O + D <= 512, "TMEM budget");
+  static constexpr int COL_S = 0;               // S of query tile x at COL_S + x*BK
+  static constexpr int COL_O = NT * BK;         // O of query tile x at COL_O + x*128
+  static_assert(COL_O + (NT - 1) * 128 + D <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 enum : int {
   B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_SFREE = B_P + 2,
-  B_PV = B_SFREE + 2, B_AFIN, B_END
+  B_PV = B_SFREE + 2, B_AFIN = B_PV + 2, B_END
 };
 static_assert(B_END <= 16, "barrier count");
 
@@ -95,22 +96,32 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
-  // ---- work item: query tile i of head h of sequence b; largest i first (longest under causal)
+  // ---- work item: query tiles 2i and 2i + 1 of head h of sequence b; largest i
+  // first (longest under causal).  Both tiles take the same K/V tiles; a CTA
+  // runs T = the larger of their KV tile counts, each tile only its own.
   const int BH = p.B * p.Hq;
-  const int nQt = (p.Nq + BQ - 1) / BQ;
-  const int i = nQt - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int nPairs = ((p.Nq + BQ - 1) / BQ + NT - 1) / NT;
+  const int i = nPairs - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const Seq sq = seq_of(p.m, b, p.status, 50);
   const int hk = h / (p.Hq / p.Hkv);                       // key/value head of the group
   const int bc = bcoord(p.m, b);                           // batch coordinate in the tensor maps
-  const int q0 = i * BQ;
+  const int q0 = i * NT * BQ;                               // first row of query tile 0
   const int nKt = (sq.nk + BK - 1) / BK;
-  const int qmax = min(q0 + BQ, sq.nq) - 1;
-  // causal: the last key any row of this tile sees is qmax + delta (none if negative)
-  const int kmax = qmax + sq.delta;
-  const int T = q0 >= sq.nq ? 0 : p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
+  // KV tiles query tile x walks: causal, up to the last key its last row sees
+  auto tiles_of = [&](int x) -> int {
+    const int qx = q0 + x * BQ;
+    const int kmax = min(qx + BQ, sq.nq) - 1 + sq.delta;
+    return qx >= sq.nq ? 0 : p.causal ? (kmax < 0 ? 0 : min(nKt, kmax / BK + 1)) : nKt;
+  };
+  int Tx[NT];
+#pragma unroll
+  for (int x = 0; x < NT; ++x) Tx[x] = tiles_of(x);
+  int T = 0;
+#pragma unroll
+  for (int x = 0; x < NT; ++x) T = max(T, Tx[x]);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
@@ -118,12 +129,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_init(bar(B_KVFULL + s), 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
     }
-    for (int j = 0; j < 2; ++j) {
-      mbar_init(bar(B_S + j), 1);
-      mbar_init(bar(B_P + j), 4);       // one arrival per softmax warp
-      mbar_init(bar(B_SFREE + j), 1);
+    for (int x = 0; x < NT; ++x) {        // per query tile
+      mbar_init(bar(B_S + x), 1);
+      mbar_init(bar(B_P + x), 4);       // one arrival per softmax warp
+      mbar_init(bar(B_SFREE + x), 1);
+      mbar_init(bar(B_PV + x), 1);
     }
-    mbar_init(bar(B_PV), 1);
     mbar_init(bar(B_AFIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -141,10 +152,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0 && T > 0) {
-      mbar_arrive_expect_tx(bar(B_Q), L::TILE);
+      mbar_arrive_expect_tx(bar(B_Q), NT * L::TILE);
 #pragma unroll
-      for (int hh = 0; hh < L::NH; ++hh)
-        tma_load_4d(sb + L::OFF_Q + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh, sq.q_start + q0, h, bc);
+      for (int x = 0; x < NT; ++x)
+#pragma unroll
+        for (int hh = 0; hh < L::NH; ++hh)
+          tma_load_4d(sb + L::OFF_Q + x * L::TILE + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh,
+                      sq.q_start + q0 + x * BQ, h, bc);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % STAGES;
@@ -169,9 +183,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (T > 0) {
       constexpr uint32_t ID_S = make_idesc_f16(128, BK, BF16, false, false);
       constexpr uint32_t ID_O = make_idesc_f16(128, D, BF16, false, true);
-      const uint32_t tO = tmem + L::COL_O;
-      const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q, 16, 1024);
-      auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BK; };
+      auto s_buf = [&](int x) -> uint32_t { return tmem + L::COL_S + x * BK; };
+      auto o_buf = [&](int x) -> uint32_t { return tmem + L::COL_O + x * 128; };
       auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_KV + (t % STAGES) * 2 * L::TILE; };
       auto kstep = [](int ks) -> uint64_t {
         return static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
@@ -180,42 +193,59 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         return __all_sync(0xffffffffu, mbar_wait(bb, parity, wc, site));
       };
       if (warp == 1) {
+        // G1: S_x = Q_x K^T for both query tiles, each once P V of its previous
+        // tile has read the P that sits in its S columns
         bool ok = wait(bar(B_Q), 0, 52);
         for (int t = 0; ok && t < T; ++t) {
-          // G1: S = Q K^T into buffer t & 1, once PV(t-2) has read the P that was there
           if (!wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1, 53)) break;
-          if (t >= 2 && !wait(bar(B_SFREE + (t & 1)), ((t - 2) >> 1) & 1, 54)) break;
-          tc_fence_after();
           const uint64_t dK_k = sw128_desc(k_tile(t), 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) umma_ss_warp(s_buf(t), dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
-          umma_commit_warp(bar(B_S + (t & 1)));
+          for (int x = 0; x < NT; ++x) {
+            if (t >= Tx[x]) continue;
+            if (t >= 1 && !wait(bar(B_SFREE + x), (t - 1) & 1, 54)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q + x * L::TILE, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_warp(s_buf(x), dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
+            umma_commit_warp(bar(B_S + x));
+          }
         }
         umma_commit_warp(bar(B_AFIN));
         drain_wait(bar(B_AFIN), 0);
       } else {
-        for (int t = 0; t < T; ++t) {
-          // PV: O += P V  (P, 16-bit, packed into the first half of its S buffer; V read MN-major)
-          if (!wait(bar(B_P + (t & 1)), (t >> 1) & 1, 55)) break;
-          tc_fence_after();
+        // PV: O_x += P_x V (P, 16-bit, packed into the first half of S_x; V read MN-major)
+        bool ok = true;
+        for (int t = 0; ok && t < T; ++t) {
           const uint64_t dV_mn = sw128_desc(k_tile(t) + L::TILE, L::HALF, 1024);
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)
-            umma_ts_warp(tO, s_buf(t) + 8 * ks, dV_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_O,
-                         (t > 0 || ks > 0));
-          umma_commit_warp(bar(B_SFREE + (t & 1)));
-          umma_commit_warp(bar(B_PV));
-          umma_commit_warp(bar(B_KVEMPTY + t % STAGES));   // G1(t) completed before P(t) existed
+          for (int x = 0; x < NT; ++x) {
+            if (t >= Tx[x]) continue;
+            if (!wait(bar(B_P + x), t & 1, 55)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              umma_ts_warp(o_buf(x), s_buf(x) + 8 * ks, dV_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_O,
+                           (t > 0 || ks > 0));
+            umma_commit_warp(bar(B_SFREE + x));
+            umma_commit_warp(bar(B_PV + x));
+          }
+          if (!ok) break;
+          umma_commit_warp(bar(B_KVEMPTY + t % STAGES));   // every G1(t) completed before its P(t) existed
         }
-        if (*abort_flag) drain_wait(bar(B_PV), (T - 1) & 1);
+        if (*abort_flag)
+          for (int x = 0; x < NT; ++x)
+            if (Tx[x] > 0) drain_wait(bar(B_PV + x), (Tx[x] - 1) & 1);
       }
     }
   } else if (warp >= 4) {
-    // ================================================================ softmax group
-    const int r = threadIdx.x - 128;                    // query row == TMEM lane
+    // ================================================================ softmax groups
+    const int qt = (warp - 4) >> 2;                     // query tile of this warpgroup
+    const int r = threadIdx.x - 128 - 128 * qt;         // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_off + L::COL_O;
-    const int q = q0 + r;
+    const uint32_t tO = tmem + lane_off + L::COL_O + qt * 128;
+    const int q = q0 + qt * BQ + r;
+    const int T = Tx[qt];
     const uint16_t* brow = nullptr;                     // this row of the bias
     if constexpr (BIAS) brow = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, q);
     float m_ref = -CUDART_INF_F;                        // reference max (log2 units); -inf: no key seen yet
@@ -228,8 +258,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       int lim = sq.nk - kv0;
       if (p.causal) lim = min(lim, q + sq.delta - kv0 + 1);
       const bool need_mask = __any_sync(0xffffffffu, lim < BK);
-      const uint32_t tS = tmem + lane_off + L::COL_S + (t & 1) * BK;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 56))) { ok = false; break; }
+      const uint32_t tS = tmem + lane_off + L::COL_S + qt * BK;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + qt), t & 1, wc, 56))) { ok = false; break; }
       tc_fence_after();
       float x[BK];
 #pragma unroll
@@ -286,7 +316,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const bool resc = !first && mt > m_ref + kRescaleThreshold;
         if (first) m_ref = mt;
         if (__any_sync(0xffffffffu, resc)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV), (t - 1) & 1, wc, 57))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV + qt), (t - 1) & 1, wc, 57))) { ok = false; break; }
           tc_fence_after();
           const float alpha = resc ? ex2_approx(m_ref - mt) : 1.f;
 #pragma unroll 1
@@ -328,12 +358,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P + (t & 1)));
+      if (lane == 0) mbar_arrive(bar(B_P + qt));
     }
     // ---- epilogue: O = acc / l (16-bit), L = (m_ref + log2 l) * ln 2
     bool have = ok && T > 0;
     if (have) {
-      have = __all_sync(0xffffffffu, mbar_wait(bar(B_PV), (T - 1) & 1, wc, 58));
+      have = __all_sync(0xffffffffu, mbar_wait(bar(B_PV + qt), (T - 1) & 1, wc, 58));
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
@@ -387,7 +417,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
   p.m = seq_map(a.pb);
-  const long long grid = static_cast<long long>((a.pb.Nq + BQ - 1) / BQ) * a.pb.B * a.pb.Hq;
+  const long long grid = static_cast<long long>(((a.pb.Nq + BQ - 1) / BQ + NT - 1) / NT) * a.pb.B * a.pb.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
