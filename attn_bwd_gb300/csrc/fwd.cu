@@ -262,11 +262,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + qt), t & 1, wc, 56))) { ok = false; break; }
       tc_fence_after();
       float x[BK];
+      if constexpr (BIAS) {
 #pragma unroll
-      for (int ch = 0; ch < BK / 32; ++ch) {
-        uint32_t sr[32];
-        tmem_ld_x32(tS + 32 * ch, sr);
-        if constexpr (BIAS) {
+        for (int ch = 0; ch < BK / 32; ++ch) {
+          uint32_t sr[32];
+          tmem_ld_x32(tS + 32 * ch, sr);
           // x = S * scale * log2(e) + bias * log2(e)
           float bv[32];
 #pragma unroll
@@ -285,15 +285,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             x[32 * ch + c] = fmaf(bv[c], 1.4426950408889634f, __uint_as_float(sr[c]) * p.scale_log2);
-        } else {
-          tmem_ld_wait();
+        }
+      } else {
+        // all four 32-column loads in flight at once, one wait
+        uint32_t sr[BK];
 #pragma unroll
-          for (int c2 = 0; c2 < 16; ++c2) {   // two columns per instruction
-            const float2 xx = f2_split(mul_f32x2(f2_bits(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1])),
-                                                 sc2));
-            x[32 * ch + 2 * c2] = xx.x;
-            x[32 * ch + 2 * c2 + 1] = xx.y;
-          }
+        for (int ch = 0; ch < BK / 32; ++ch) tmem_ld_x32(tS + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * ch));
+        tmem_ld_wait();
+#pragma unroll
+        for (int c2 = 0; c2 < BK / 2; ++c2) {   // two columns per instruction
+          const float2 xx = f2_split(mul_f32x2(f2_bits(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1])), sc2));
+          x[2 * c2] = xx.x;
+          x[2 * c2 + 1] = xx.y;
         }
       }
       // row max over eight independent partial maxima (a single running max is a
