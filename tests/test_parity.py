@@ -249,3 +249,27 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert _lib.fa_last_device_error(s) == _lib.FA_ERR_DEVICE_TIMEOUT
     assert _lib.fa_last_device_error(s) == _lib.FA_OK        # read-and-clear
     check_full(inputs.tiny_mha()[0], 1, False)              # the context still works
+
+
+def test_llama_gqa_sampled_deterministic_headline():
+    """The deterministic path at the benchmark's shape: full run on the GPU, two (batch, kv-head)
+    groups computed exactly by the oracle; and a second run is bitwise identical."""
+    shape = inputs.llama_gqa(8192)
+    q, k, v, do = inputs.draw(shape, 15, device="cuda")
+    o, lse, dq, dk, dv = gpu_run(q, k, v, do, shape, True)
+    G = shape.Hq // shape.Hkv
+    pairs = {}
+    for b, g in [(1, 2), (shape.B - 1, 0)]:
+        hs = slice(g * G, (g + 1) * G)
+        sl = lambda t, h: t[b:b + 1, h].cpu()  # noqa: E731
+        qs, dos = sl(q, hs), sl(do, hs)
+        ks, vs = sl(k, slice(g, g + 1)), sl(v, slice(g, g + 1))
+        r = attn_ref.backward(qs, ks, vs, dos, shape.softmax_scale, True)
+        pairs[f"dQ[{b},{g}]"] = (_np(dq[b:b + 1, hs]), r["dq"])
+        pairs[f"dK[{b},{g}]"] = (_np(dk[b:b + 1, g:g + 1]), r["dk"])
+        pairs[f"dV[{b},{g}]"] = (_np(dv[b:b + 1, g:g + 1]), r["dv"])
+    fails, rep = errors(pairs)
+    assert not fails, rep
+    again = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, True, True)
+    torch.cuda.synchronize()
+    assert torch.equal(again[0], dq) and torch.equal(again[1], dk) and torch.equal(again[2], dv)

@@ -92,3 +92,35 @@ def test_out_of_range_offsets_are_reported_not_used():
     # sequence 0 (rows 0..69 here, since its offsets read 0..70) was computed against keys 0..39
     assert np.abs(_np(o[:, :70]) - o_ref).max() <= REL * np.abs(o_ref).max() + ABS
     test_packed_batch(inputs.packed_mix()[1], False)                      # the context still works
+
+
+def test_packed_batch_at_benchmark_scale_sampled():
+    """The packed workload bench.py --feature varlen times (16 causal sequences of 768..7936
+    tokens, Llama-3 heads): full run on the GPU, three sequences of one kv-head group checked
+    exactly by the oracle."""
+    import random
+    rnd = random.Random(7)
+    lens = [rnd.randrange(512, 8193, 64) for _ in range(16)]
+    pk = inputs.Packed(tuple(lens), tuple(lens), 32, 8, 128, 1, "bf16")
+    q, k, v, do = inputs.draw_packed(pk, 7, device="cuda")
+    o, lse = torch_api.forward_varlen(q, k, v, pk.cu_q, pk.cu_k, pk.softmax_scale, 1)
+    dq, dk, dv = torch_api.backward_varlen(q, k, v, o, do, lse, pk.cu_q, pk.cu_k, pk.softmax_scale, 1, False)
+    torch.cuda.synchronize()
+    assert _lib.fa_last_device_error() == _lib.FA_OK
+    cu = pk.cu_q
+    g, G = 3, 4
+    hs = slice(g * G, (g + 1) * G)
+    pairs = {}
+    for b in (0, 12, 15):                       # lengths 3136, 7936 and 768
+        rows = slice(cu[b], cu[b + 1])
+        qs, dos = q[hs, rows].cpu()[None], do[hs, rows].cpu()[None]
+        ks, vs = k[g:g + 1, rows].cpu()[None], v[g:g + 1, rows].cpu()[None]
+        o_ref, l_ref = attn_ref.forward(qs, ks, vs, pk.softmax_scale, 1)
+        r = attn_ref.backward(qs, ks, vs, dos, pk.softmax_scale, 1)
+        pairs[f"O[{b}]"] = (_np(o[hs, rows])[None], o_ref)
+        pairs[f"L[{b}]"] = (_np(lse[hs, rows])[None], l_ref)
+        pairs[f"dQ[{b}]"] = (_np(dq[hs, rows])[None], r["dq"])
+        pairs[f"dK[{b}]"] = (_np(dk[g:g + 1, rows])[None], r["dk"])
+        pairs[f"dV[{b}]"] = (_np(dv[g:g + 1, rows])[None], r["dv"])
+    fails, rep = _compare(pairs)
+    assert not fails, rep
