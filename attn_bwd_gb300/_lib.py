@@ -69,8 +69,9 @@ _SIGNATURES = {
                             _F, _I, _I, _P]),
     "fa_bwd_strided": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(fa_strides), _P, _P, _I, _I, _I, _I,
                             _I, _I, _I, _I, _F, _I, _I, _I, _P, _S, _P]),
-    "fa_bwd_host_staging_size": (_S, [_I, _I, _I, _I, _I, _I, _I, _I]),
-    "fa_bwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_host_staging_size": (_S, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "fa_bwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P, _S,
+                         _P]),
     "fa_fwd_bias": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(fa_bias), ctypes.POINTER(fa_strides), _P, _P, _I, _I,
                          _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "fa_bwd_bias": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(fa_bias), ctypes.POINTER(fa_strides),
@@ -78,6 +79,7 @@ _SIGNATURES = {
 }
 
 FA_STATIC_SCRATCH_BYTES = 64 << 20
+FA_HOST_MAX_SLOTS = 8
 
 _lib = None
 
@@ -242,13 +244,13 @@ def fa_bwd_bias(q, k, v, o, dO, lse, dq, dk, dv, bias, strides, cu_q, cu_k, B, H
                               _stream(stream))
 
 
-def fa_bwd_host_staging_size(B, Hq, Hkv, Nq, Nkv, d, deterministic, chunk_b) -> int:
-    return load().fa_bwd_host_staging_size(B, Hq, Hkv, Nq, Nkv, d, int(deterministic), int(chunk_b))
+def fa_bwd_host_staging_size(B, Hq, Hkv, Nq, Nkv, d, deterministic, chunk_groups, slots) -> int:
+    return load().fa_bwd_host_staging_size(B, Hq, Hkv, Nq, Nkv, d, int(deterministic), int(chunk_groups), int(slots))
 
 
 def fa_bwd_host(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic,
-                chunk_b, staging, staging_bytes, stream=None) -> int:
+                chunk_groups, slots, staging, staging_bytes, stream=None) -> int:
     """fa_bwd on HOST tensors (pinned for overlap), pipelined through device staging memory."""
     return load().fa_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                               B, Hq, Hkv, Nq, Nkv, d, float(scale), int(causal), int(dtype), int(deterministic),
-                              int(chunk_b), _ptr(staging), int(staging_bytes), _stream(stream))
+                              int(chunk_groups), int(slots), _ptr(staging), int(staging_bytes), _stream(stream))

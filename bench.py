@@ -39,6 +39,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention backward TFLOP/s (bf16/fp16) and % of GB300 dense tensor peak"
 PEAKS_FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# fa_bwd_host pipeline of the e2e leg: (batch, kv-head) groups per chunk, staging slots
+HOST_CHUNK_GROUPS = 4
+HOST_SLOTS = 4
 
 
 def parse():
@@ -368,19 +371,19 @@ def main():
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region:
     # fa_bwd_host takes the host tensors and overlaps their transfers with the computation,
-    # one sequence of the batch per chunk
+    # in chunks of (batch, kv-head) groups through a ring of device staging slots
     host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     e2e_steps = max(3, args.steps // 4)
-    chunk_b = 1
-    st_bytes = _lib.fa_bwd_host_staging_size(B, Hq, Hkv, N, N, d, det, chunk_b)
+    chunk_groups, slots = HOST_CHUNK_GROUPS, HOST_SLOTS
+    st_bytes = _lib.fa_bwd_host_staging_size(B, Hq, Hkv, N, N, d, det, chunk_groups, slots)
     staging = torch.empty(st_bytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        st = _lib.fa_bwd_host(*host_in, *host_out, B, Hq, Hkv, N, N, d, scale, causal, dt_code, det, chunk_b,
-                              staging, st_bytes, stream)
+        st = _lib.fa_bwd_host(*host_in, *host_out, B, Hq, Hkv, N, N, d, scale, causal, dt_code, det, chunk_groups,
+                              slots, staging, st_bytes, stream)
         if st:
             raise RuntimeError(f"fa_bwd_host failed: {st}")
 
@@ -411,7 +414,8 @@ def main():
         "kernel_ms": {"bwd_main_avg": main_avg, "bwd_main_min": min(main_ms),
                       "other_avg": ms_total / args.steps - main_avg},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "fa_bwd_host (pinned host tensors, transfers overlapped in batch chunks of 1)"},
+                "api": f"fa_bwd_host (pinned host tensors, transfers overlapped in chunks of {chunk_groups} "
+                       f"(batch, kv-head) groups through {slots} staging slots)"},
         "gpu_launches": 3 * args.steps,
         "forward": {"kernel": "fwd_kernel (makes O and L; outside the timed step)", "ms": fwd_ms,
                     "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,

@@ -41,8 +41,9 @@
  * fa_bwd_host), 16-byte aligned.  The caller owns every buffer (inputs,
  * outputs, workspace, staging) and the stream; the library allocates no
  * device memory, keeps no state besides one status word per kernel family
- * (and fa_bwd_host's copy streams), and never synchronises inside fa_fwd* /
- * fa_bwd*.  All work is enqueued on `stream`.
+ * (and fa_bwd_host's copy and slot streams), and never synchronises inside
+ * fa_fwd* / fa_bwd*.  All work is enqueued on `stream` (fa_bwd_host forks
+ * from it and joins back into it).
  *
  * Errors: each call validates its arguments first and, on failure, returns a
  * non-zero fa_status WITHOUT launching anything.  FA_ERR_CUDA reports a
@@ -321,25 +322,41 @@ int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, cons
  * fa_bwd_host -- fa_bwd for tensors in HOST memory (same layouts, contiguous),
  * with the transfers overlapped with the computation.  The pages have no
  * counterpart; it serves callers whose activations live in host memory (for
- * example offloaded between the forward and the backward).  The batch is cut
- * into chunks of chunk_b sequences that flow through two slots of the caller's
- * DEVICE staging memory: while a chunk computes on `stream`, the next one is
- * copied in and the previous one copied out on two copy streams the library
- * creates once per device.  The call returns once everything is queued; the
- * work is complete, dq/dk/dv written in host memory, when `stream` reaches
- * this point.  Host buffers should be page-locked (cudaHostAlloc /
- * cudaHostRegister); pageable memory works but serialises the copies.
- * staging: >= fa_bwd_host_staging_size(...) bytes, 256-byte aligned, not used
- * by anything else until `stream` passes the call.  chunk_b in [1, B].
+ * example offloaded between the forward and the backward).
+ *
+ * The problem is cut into chunks of `chunk_groups` (batch, kv-head) groups
+ * (a group is one key/value head of one sequence with its Hq/Hkv query heads;
+ * groups are numbered b*Hkv + hkv, and a run of them is contiguous in every
+ * tensor).  Chunks flow through a ring of `slots` slots of the caller's DEVICE
+ * staging memory: one copy stream brings chunk inputs in, chunk c computes on
+ * the stream of slot c % slots once its inputs are in, and a second copy
+ * stream takes dQ, dK, dV out; a slot is refilled once its previous chunk has
+ * been copied out.  The copy streams and FA_HOST_MAX_SLOTS slot streams are
+ * created by the library once per device.  Results equal fa_bwd's on the same
+ * values (dK, dV and deterministic dQ bitwise).
+ *
+ * The call returns once everything is queued; the work is complete, dq/dk/dv
+ * written in host memory, when `stream` reaches this point.  Host buffers
+ * should be page-locked (cudaHostAlloc / cudaHostRegister); pageable memory
+ * works but serialises the copies.  Small chunks shorten the exposed first
+ * copy-in and last copy-out; enough slots keep the copy-in stream from waiting
+ * (with the link slower than the computation, 3-4 slots suffice).
+ *
+ * chunk_groups in [1, B*Hkv], slots in [1, FA_HOST_MAX_SLOTS] (FA_ERR_SHAPE
+ * otherwise).  staging: >= fa_bwd_host_staging_size(...) bytes (0 for invalid
+ * arguments), 256-byte aligned (FA_ERR_ALIGN), not used by anything else until
+ * `stream` passes the call (FA_ERR_WORKSPACE if NULL or too small).
  */
+#define FA_HOST_MAX_SLOTS 8
+
 size_t fa_bwd_host_staging_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int deterministic,
-                                int chunk_b);
+                                int chunk_groups, int slots);
 
 int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dO,
                 const float* lse, void* dq, void* dk, void* dv,
                 int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int causal,
-                int dtype, int deterministic, int chunk_b, void* staging, size_t staging_bytes,
-                cudaStream_t stream);
+                int dtype, int deterministic, int chunk_groups, int slots,
+                void* staging, size_t staging_bytes, cudaStream_t stream);
 
 /* Human-readable name of an fa_status value (static string, never NULL). */
 const char* fa_strerror(int status);

@@ -218,15 +218,24 @@ def test_fwd_bias_takes_no_dbias(lib):
 
 
 def test_host_pipeline_validation_and_staging_size(lib):
-    one = _lib.fa_bwd_workspace_size(2, 4, 2, 100, 100, 64, 0)
+    # 5 sequences x 2 kv heads = 10 (batch, kv-head) groups of 2 query heads each
+    one = _lib.fa_bwd_workspace_size(1, 2 * 3, 3, 100, 100, 64, 0)
     assert one > 0
-    two_slots = _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 2)
-    one_slot = _lib.fa_bwd_host_staging_size(2, 4, 2, 100, 100, 64, 0, 2)
-    assert two_slots == 2 * one_slot and one_slot > one
-    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 0) == 0
-    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 6) == 0
+    slot = _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 3, 1)
+    assert slot > one
+    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 3, 2) == 2 * slot
+    # never more slots than chunks: 10 groups in chunks of 3 -> 4 chunks
+    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 3, 8) == 4 * slot
+    assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 10, 8) == \
+        _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, 10, 1)
+    for cg, sl in ((0, 2), (11, 2), (3, 0), (3, _lib.FA_HOST_MAX_SLOTS + 1)):
+        assert _lib.fa_bwd_host_staging_size(5, 4, 2, 100, 100, 64, 0, cg, sl) == 0
+    assert _lib.fa_bwd_host_staging_size(5, 4, 3, 100, 100, 64, 0, 1, 2) == 0    # Hq % Hkv != 0
     args = [A] * 9 + [5, 4, 2, 100, 100, 64, 0.1, 1, _lib.FA_BF16, 0]
-    assert _lib.fa_bwd_host(*args, 0, W, 1 << 30) == _lib.FA_ERR_SHAPE
-    assert _lib.fa_bwd_host(*args, 2, None, 1 << 30) == _lib.FA_ERR_WORKSPACE
-    assert _lib.fa_bwd_host(*args, 2, W, 100) == _lib.FA_ERR_WORKSPACE
-    assert _lib.fa_bwd_host(*args, 2, W + 16, 1 << 30) == _lib.FA_ERR_ALIGN
+    assert _lib.fa_bwd_host(*args, 0, 2, W, 1 << 30) == _lib.FA_ERR_SHAPE
+    assert _lib.fa_bwd_host(*args, 2, 0, W, 1 << 30) == _lib.FA_ERR_SHAPE
+    assert _lib.fa_bwd_host(*args, 2, 2, None, 1 << 30) == _lib.FA_ERR_WORKSPACE
+    assert _lib.fa_bwd_host(*args, 2, 2, W, 100) == _lib.FA_ERR_WORKSPACE
+    assert _lib.fa_bwd_host(*args, 2, 2, W + 16, 1 << 30) == _lib.FA_ERR_ALIGN
+    bad = [A] * 9 + [5, 4, 3, 100, 100, 64, 0.1, 1, _lib.FA_BF16, 0]
+    assert _lib.fa_bwd_host(*bad, 1, 2, W, 1 << 30) == _lib.FA_ERR_GQA
