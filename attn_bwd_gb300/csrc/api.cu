@@ -72,6 +72,32 @@ int make_map(CUtensorMap* m, const void* base, int bf16, int d, int rows, int he
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 4-D view (keys, queries, heads, batch) of a 16-bit bias (or dBias) with element strides s
+// for the query, head and batch axes (0 broadcasts); box = box_k keys x box_q
+// queries of one head and sequence: 128 keys unswizzled (256-byte rows in shared
+// memory) or 64 keys with the 128-byte swizzle.  A broadcast axis gets extent 1
+// (so it is addressed at coordinate 0) and a stride that is never used; keys
+// past Nkv and queries past Nq read as zero (and are not written by a store).
+int make_bias_map(CUtensorMap* m, const void* base, int bf16, int Nkv, int Nq, int Hq, int B, Str3 s, int box_k,
+                  int box_q) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(Nkv), static_cast<cuuint64_t>(s.n ? Nq : 1),
+                              static_cast<cuuint64_t>(s.h ? Hq : 1), static_cast<cuuint64_t>(s.b ? B : 1)};
+  // a broadcast axis takes the stride of a dense layout (capped; it is never stepped)
+  const cuuint64_t cap = 1ull << 39;
+  const cuuint64_t rq = s.n ? static_cast<cuuint64_t>(s.n) * 2 : (static_cast<cuuint64_t>(Nkv) * 2 + 15) / 16 * 16;
+  const cuuint64_t rh = s.h ? static_cast<cuuint64_t>(s.h) * 2 : (rq * dims[1] < cap ? rq * dims[1] : cap);
+  const cuuint64_t rb = s.b ? static_cast<cuuint64_t>(s.b) * 2 : (rh * dims[2] < cap ? rh * dims[2] : cap);
+  const cuuint64_t strides[3] = {rq, rh, rb};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_q), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              box_k == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 int check_shape(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int dtype) {
@@ -252,7 +278,10 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   if ((st = map_q(&tq, q, g.st.q, bf, g, 128))) return st;
   if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
   if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
-  return cuda_status(launch_fwd(a, tq, tk, tv, status, stream));
+  CUtensorMap tb{};
+  if (g.bias != nullptr && (st = make_bias_map(&tb, g.bias, bf, g.Nkv, g.Nq, g.Hq, g.B, g.bias_st, 64, 128)))
+    return st;
+  return cuda_status(launch_fwd(a, tq, tk, tv, tb, status, stream));
 }
 
 int run_preprocess(const Geo& g, const void* o, const void* dO, const float* lse, int dtype, int deterministic,
@@ -292,9 +321,14 @@ int run_main(const Geo& g, const void* q, const void* k, const void* v, const vo
   if ((st = map_q(&tdo, dO, g.st.dO, bf, g, 64))) return st;
   if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
   if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
+  CUtensorMap tb{}, tdb{};
+  if (g.bias != nullptr && (st = make_bias_map(&tb, g.bias, bf, g.Nkv, g.Nq, g.Hq, g.B, g.bias_st, 128, kMainBM)))
+    return st;
+  if (g.dbias != nullptr && (st = make_bias_map(&tdb, g.dbias, bf, g.Nkv, g.Nq, g.Hq, g.B, g.dbias_st, 128, 32)))
+    return st;
   if (a.pb.dbias != nullptr && a.pb.causal)
     if ((st = cuda_status(launch_dbias_zero(a.pb, a.status, stream)))) return st;
-  return cuda_status(launch_bwd_main(a, tq, tdo, tk, tv, stream));
+  return cuda_status(launch_bwd_main(a, tq, tdo, tk, tv, tb, tdb, stream));
 }
 
 int run_dq(const Geo& g, const void* q, const void* k, const void* v, const void* dO, void* dq, float scale,

@@ -25,6 +25,8 @@
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer: K, V once; Q, dO, L, D tiles through a 4-stage ring
+//                (3 stages with an additive bias, whose [64 query x 128 key]
+//                tiles then flow through a 2-stage ring of their own)
 //   warp 1       owns TMEM; one lane issues every tcgen05.mma
 //   warps 4-11   two "softmax" groups: thread r of group w owns KV row r (TMEM
 //                lane r) and query columns [32w, 32w+32) of each tile; P, dS
@@ -56,12 +58,15 @@ namespace {
 
 constexpr int BN = kMainBN;   // KV rows per CTA (TMEM lanes)
 constexpr int BM = kMainBM;   // query rows per tile
-constexpr int STAGES = 4;     // Q/dO ring depth: loads run ~2 tiles ahead of use
+constexpr int BSTAGES = 2;    // bias tiles in flight (with an additive bias)
 constexpr int kThreads = 512;
 constexpr int kGroupChunk = 32;   // (batch, kv-head) groups per launch-order chunk
 
-template <int D>
+template <int D, bool BIAS>
 struct Layout {
+  // Q/dO ring depth: loads run ~2 tiles ahead of use.  With a bias, one stage
+  // makes room for the bias ring (two [BM query][BN key] tiles).
+  static constexpr int STAGES = BIAS ? 3 : 4;
   static constexpr int NH = D / 64;               // 64-column halves of a row
   static constexpr int KHALF = BN * 128;          // bytes of one half of a K/V tile
   static constexpr int QHALF = BM * 128;          // bytes of one half of a Q/dO tile
@@ -73,10 +78,14 @@ struct Layout {
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_BYTES;
   static constexpr int DS_BYTES = BN * BM * 2;    // dS^T, 128 rows x 128 B
-  static constexpr int OFF_LD = OFF_DS + DS_BYTES;
+  static constexpr int OFF_BIAS = OFF_DS + DS_BYTES;
+  static constexpr int BIAS_BYTES = BM * BN * 2;  // bias of one tile: BM rows (queries) of BN keys, 256 B each
+  static constexpr int OFF_DB = OFF_BIAS + (BIAS ? BSTAGES * BIAS_BYTES : 0);
+  static constexpr int DB_HALF = 32 * BN * 2;     // dBias of one softmax group's 32 queries
+  static constexpr int OFF_LD = OFF_DB + (BIAS ? 2 * DB_HALF : 0);
   static constexpr int LD_BYTES = 2 * BM * 4;     // -L*log2e and D of one tile
   static constexpr int OFF_BAR = OFF_LD + STAGES * LD_BYTES;
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = TOTAL + 1024;      // slack for 1024-byte alignment
@@ -91,15 +100,16 @@ struct Layout {
   static_assert(COL_DQ + BM <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
-static_assert((STAGES & (STAGES - 1)) == 0, "ring depth must be a power of two");
-
 // barrier indices
 // (S and P have one barrier per S^T buffer: tile t uses buffer t & 1)
-enum : int {
-  B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_SFREE = B_P + 2,
-  B_DP = B_SFREE + 2, B_DPFREE, B_DS, B_DQFULL, B_DQEMPTY, B_DSFREE, B_ACC, B_AFIN, B_END
+template <int STAGES>
+struct Bars {
+  static constexpr int KV = 0, QFULL = 1, QEMPTY = 1 + STAGES, S = 1 + 2 * STAGES, P = S + 2, SFREE = P + 2,
+                       DP = SFREE + 2, DPFREE = DP + 1, DS = DP + 2, DQFULL = DP + 3, DQEMPTY = DP + 4,
+                       DSFREE = DP + 5, ACC = DP + 6, AFIN = DP + 7, BFULL = DP + 8, BEMPTY = BFULL + BSTAGES,
+                       DBFULL = BEMPTY + BSTAGES, DBFREE = DBFULL + 2, END = DBFREE + 2;
 };
-static_assert(B_END <= 24, "barrier count");
+static_assert(Bars<4>::END <= Layout<128, false>::NBAR && Bars<3>::END <= Layout<128, true>::NBAR, "barrier count");
 
 struct Params {
   const float* nLg;
@@ -136,8 +146,14 @@ template <int D, bool BF16, bool DET, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_bias, const __grid_constant__ CUtensorMap tm_dbias,
                 const Params p) {
-  using L = Layout<D>;
+  using L = Layout<D, BIAS>;
+  using BR = Bars<L::STAGES>;
+  constexpr int STAGES = L::STAGES;
+  // ring stage and phase of tile t
+  auto stg = [](int t) -> int { return static_cast<int>(static_cast<unsigned>(t) % STAGES); };
+  auto rph = [](int t) -> uint32_t { return (static_cast<unsigned>(t) / STAGES) & 1u; };
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled tiles.  Offsetting the array itself
   // (not a rounded integer) keeps the pointer in the shared address space, so
@@ -178,24 +194,32 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int T = kv0 < sq.nk ? G * per_head : 0;       // tiles this CTA processes
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_KV), 1);
+    mbar_init(bar(BR::KV), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_QFULL + s), 1);
-      mbar_init(bar(B_QEMPTY + s), 1);
+      mbar_init(bar(BR::QFULL + s), 1);
+      mbar_init(bar(BR::QEMPTY + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_S + i), 1);
-      mbar_init(bar(B_P + i), 8);        // one arrival per softmax warp
-      mbar_init(bar(B_SFREE + i), 1);
+      mbar_init(bar(BR::S + i), 1);
+      mbar_init(bar(BR::P + i), 8);        // one arrival per softmax warp
+      mbar_init(bar(BR::SFREE + i), 1);
     }
-    mbar_init(bar(B_AFIN), 1);
-    mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_DPFREE), 8);
-    mbar_init(bar(B_DS), 8);
-    mbar_init(bar(B_DQFULL), 1);
-    mbar_init(bar(B_DQEMPTY), 4);      // one arrival per dQ warp
-    mbar_init(bar(B_DSFREE), 1);
-    mbar_init(bar(B_ACC), 1);
+    mbar_init(bar(BR::AFIN), 1);
+    mbar_init(bar(BR::DP), 1);
+    mbar_init(bar(BR::DPFREE), 8);
+    mbar_init(bar(BR::DS), 8);
+    mbar_init(bar(BR::DQFULL), 1);
+    mbar_init(bar(BR::DQEMPTY), 4);      // one arrival per dQ warp
+    mbar_init(bar(BR::DSFREE), 1);
+    mbar_init(bar(BR::ACC), 1);
+    for (int i = 0; i < BSTAGES; ++i) {
+      mbar_init(bar(BR::BFULL + i), 1);
+      mbar_init(bar(BR::BEMPTY + i), 8);   // one arrival per softmax warp
+    }
+    for (int g = 0; g < 2; ++g) {          // dBias block of softmax group g
+      mbar_init(bar(BR::DBFULL + g), 4);   // written: one arrival per warp of the group
+      mbar_init(bar(BR::DBFREE + g), 1);   // read out by the previous store
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -213,21 +237,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ================================================================ TMA producer
     if (lane == 0 && T > 0) {
       const int bc = bcoord(p.m, b);                      // batch coordinate in the tensor maps
-      mbar_arrive_expect_tx(bar(B_KV), 2 * L::KV_BYTES);
+      mbar_arrive_expect_tx(bar(BR::KV), 2 * L::KV_BYTES);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
-        tma_load_4d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(B_KV), 64 * hh, sq.k_start + kv0, hkv, bc);
-        tma_load_4d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(B_KV), 64 * hh, sq.k_start + kv0, hkv, bc);
+        tma_load_4d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(BR::KV), 64 * hh, sq.k_start + kv0, hkv, bc);
+        tma_load_4d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(BR::KV), 64 * hh, sq.k_start + kv0, hkv, bc);
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % STAGES;
-        const uint32_t ph = (t / STAGES) & 1;
-        if (t >= STAGES && !mbar_wait(bar(B_QEMPTY + s), ph ^ 1, wc, 1)) break;
+        const int s = stg(t);
+        const uint32_t ph = rph(t);
+        if (t >= STAGES && !mbar_wait(bar(BR::QEMPTY + s), ph ^ 1, wc, 1)) break;
         const int h = hkv * G + t / per_head;
         const int q0 = (i0 + t % per_head) * BM;
         const int bh = b * p.Hq + h;                      // workspace rows are (b, h, padded q)
-        const uint32_t fb = bar(B_QFULL + s);
+        const uint32_t fb = bar(BR::QFULL + s);
         mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + L::LD_BYTES);
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
@@ -238,12 +262,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const size_t row = static_cast<size_t>(bh) * p.NqPad + q0;
         bulk_load(sb + L::OFF_LD + s * L::LD_BYTES, p.nLg + row, BM * 4, fb);
         bulk_load(sb + L::OFF_LD + s * L::LD_BYTES + BM * 4, p.Dv + row, BM * 4, fb);
+        if constexpr (BIAS) {
+          // bias of (query rows q0.., keys kv0..) of head h, sequence b: a broadcast axis
+          // has extent 1 in the map and is addressed at 0
+          const int bs = t & (BSTAGES - 1);
+          if (t >= BSTAGES && !mbar_wait(bar(BR::BEMPTY + bs), ((t / BSTAGES) & 1) ^ 1, wc, 17)) break;
+          const uint32_t bb = bar(BR::BFULL + bs);
+          mbar_arrive_expect_tx(bb, L::BIAS_BYTES);
+          tma_load_4d(sb + L::OFF_BIAS + bs * L::BIAS_BYTES, &tm_bias, bb, kv0, p.m.bias_st.n ? q0 : 0,
+                      p.m.bias_st.h ? h : 0, p.m.bias_st.b ? b : 0);
+        }
         issued = t + 1;
       }
       // Never leave a copy in flight into shared memory this CTA is about to release.
-      drain_wait(bar(B_KV), 0);
+      drain_wait(bar(BR::KV), 0);
       for (int t = max(0, issued - STAGES); t < issued; ++t)
-        drain_wait(bar(B_QFULL + t % STAGES), (t / STAGES) & 1);
+        drain_wait(bar(BR::QFULL + stg(t)), rph(t));
+      if constexpr (BIAS)
+        for (int t = max(0, issued - BSTAGES); t < issued; ++t)
+          drain_wait(bar(BR::BFULL + (t & (BSTAGES - 1))), (t / BSTAGES) & 1);
     }
   } else if (warp == 1 || warp == 2) {
     // ================================================================ MMA issuers
@@ -263,8 +300,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t tdK = tmem + L::COL_DK, tdV = tmem + L::COL_DV, tdQ = tmem + L::COL_DQ;
       const uint32_t aK = sb + L::OFF_K, aV = sb + L::OFF_V;
       auto s_buf = [&](int t) -> uint32_t { return tmem + L::COL_S + (t & 1) * BM; };
-      auto q_tile = [&](int t) -> uint32_t { return sb + L::OFF_Q + (t & (STAGES - 1)) * L::Q_BYTES; };
-      auto do_tile = [&](int t) -> uint32_t { return sb + L::OFF_DO + (t & (STAGES - 1)) * L::Q_BYTES; };
+      auto q_tile = [&](int t) -> uint32_t { return sb + L::OFF_Q + stg(t) * L::Q_BYTES; };
+      auto do_tile = [&](int t) -> uint32_t { return sb + L::OFF_DO + stg(t) * L::Q_BYTES; };
       // Each operand tile's descriptor is built once and stepped by
       // compile-time offsets (the start address is the descriptor's low field,
       // so adding offset >> 4 advances it).
@@ -285,11 +322,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       };
 
       if (warp == 1) {
-        bool ok = wait(bar(B_KV), 0, 2);
+        bool ok = wait(bar(BR::KV), 0, 2);
         for (int t = 0; ok && t < T; ++t) {
           // G1: S^T(t) = K Q^T  (contraction over d, 16 per instruction), into buffer t & 1
-          if (!wait(bar(B_QFULL + (t & (STAGES - 1))), (t / STAGES) & 1, 3)) break;
-          if (t >= 2 && !wait(bar(B_SFREE + (t & 1)), ((t - 2) >> 1) & 1, 15)) break;
+          if (!wait(bar(BR::QFULL + stg(t)), rph(t), 3)) break;
+          if (t >= 2 && !wait(bar(BR::SFREE + (t & 1)), ((t - 2) >> 1) & 1, 15)) break;
           tc_fence_after();
           {
             const uint64_t dQ_k = sw128_desc(q_tile(t), 16, 1024);
@@ -297,26 +334,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
               umma_ss_warp(tS, dK_k + kstep(ks, L::KHALF), dQ_k + kstep(ks, L::QHALF), ID_S, ks > 0);
-            umma_commit_warp(bar(B_S + (t & 1)));
+            umma_commit_warp(bar(BR::S + (t & 1)));
           }
           // G2: dP^T(t) = V dO^T, once the softmax groups have loaded dP^T(t-1)
-          if (t >= 1 && !wait(bar(B_DPFREE), (t - 1) & 1, 14)) break;
+          if (t >= 1 && !wait(bar(BR::DPFREE), (t - 1) & 1, 14)) break;
           tc_fence_after();
           {
             const uint64_t dO_k = sw128_desc(do_tile(t), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
               umma_ss_warp(tdP, dV_k + kstep(ks, L::KHALF), dO_k + kstep(ks, L::QHALF), ID_S, ks > 0);
-            umma_commit_warp(bar(B_DP));
+            umma_commit_warp(bar(BR::DP));
           }
         }
         // this warp's MMAs must have completed before TMEM is released
-        umma_commit_warp(bar(B_AFIN));
-        drain_wait(bar(B_AFIN), 0);
+        umma_commit_warp(bar(BR::AFIN));
+        drain_wait(bar(BR::AFIN), 0);
       } else {
         for (int t = 0; t < T; ++t) {
           // G3: dV += P^T dO  (P^T from TMEM; contraction over the BM query rows)
-          if (!wait(bar(B_P + (t & 1)), (t >> 1) & 1, 4)) break;
+          if (!wait(bar(BR::P + (t & 1)), (t >> 1) & 1, 4)) break;
           tc_fence_after();
           {
             const uint32_t tS = s_buf(t);
@@ -324,10 +361,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int ks = 0; ks < BM / 16; ++ks)
               umma_ts_warp(tdV, tS + a_col(ks), dO_mn + mnstep(ks), ID_KV, (t > 0 || ks > 0));
-            umma_commit_warp(bar(B_SFREE + (t & 1)));
+            umma_commit_warp(bar(BR::SFREE + (t & 1)));
           }
           // G4: dK += dS^T Q  (dS^T from its smem tile, K-major; contraction over the query rows)
-          if (!wait(bar(B_DS), t & 1, 5)) break;
+          if (!wait(bar(BR::DS), t & 1, 5)) break;
           tc_fence_after();
           {
             const uint64_t dQ_mn = sw128_desc(q_tile(t), L::QHALF, 1024);
@@ -339,19 +376,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if constexpr (!DET) {
             // G5: dQ^T = K^T dS^T  (contraction over the BN key rows); M = 128 covers d
             // (for d = 64 the upper 64 lanes are unused)
-            if (t > 0 && !wait(bar(B_DQEMPTY), (t - 1) & 1, 6)) break;
+            if (t > 0 && !wait(bar(BR::DQEMPTY), (t - 1) & 1, 6)) break;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks)
               umma_ss_warp(tdQ, dK_mn + mnstep(ks), dS_mn + mnstep(ks), ID_Q, ks > 0);
-            umma_commit_warp(bar(B_DQFULL));
+            umma_commit_warp(bar(BR::DQFULL));
           }
-          umma_commit_warp(bar(B_DSFREE));
+          umma_commit_warp(bar(BR::DSFREE));
           // stage of tile t: G1/G2(t) have completed (P(t), dS(t) depend on them), G3/G4(t) are tracked here
-          umma_commit_warp(bar(B_QEMPTY + (t & (STAGES - 1))));
+          umma_commit_warp(bar(BR::QEMPTY + stg(t)));
         }
-        umma_commit_warp(bar(B_ACC));
-        if (*abort_flag) drain_wait(bar(B_ACC), 0);
+        umma_commit_warp(bar(BR::ACC));
+        if (*abort_flag) drain_wait(bar(BR::ACC), 0);
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -366,16 +403,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
     int qi = i0;                                          // query tile of tile t (walked, no division)
     int h = hkv * G;                                      // and its query head
+    const bool db_lead = (threadIdx.x & 127) == 0;        // issues this group's dBias stores
+    int n_db = 0;                                         // dBias blocks this group has stored by TMA
     for (int t = 0; t < T; ++t, h += (qi + 1 == nQt), qi = (qi + 1 == nQt) ? i0 : qi + 1) {
-      const int s = t & (STAGES - 1);
+      const int s = stg(t);
       const int q0 = qi * BM;
       const int qc = q0 + 32 * grp;                       // query of this group's column 0
-      float bv[32];                                       // bias of (query qc + c, key kv)
+      // bias of (query qc + c, key kv): from the tile the producer staged (row = query,
+      // 256-byte rows of keys, so a warp reads 64 contiguous bytes per query), read
+      // four columns at a time where they are used; queries past the sequence read 0
+      const uint16_t* bcol = nullptr;
+      int bstep = 0, bvalid = 0;
       if constexpr (BIAS) {
-        const uint16_t* bcol = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, qc) + kv;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          bv[c] = (row_ok && qc + c < sq.nq) ? half_to_float<BF16>(__ldg(bcol + c * p.m.bias_st.n)) : 0.f;
+        const int bs = t & (BSTAGES - 1);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::BFULL + bs), (t / BSTAGES) & 1, wc, 16))) break;
+        const bool qbc = p.m.bias_st.n == 0;
+        bcol = reinterpret_cast<const uint16_t*>(smem + L::OFF_BIAS + bs * L::BIAS_BYTES) + r +
+               (qbc ? 0 : 32 * grp * BN);
+        bstep = qbc ? 0 : BN;
+        bvalid = sq.nq - qc;
       }
       const float* Ls = reinterpret_cast<const float*>(smem + L::OFF_LD + s * L::LD_BYTES) + 32 * grp;
       const float* Ds = Ls + BM;
@@ -385,7 +431,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // the decision is made once per warp.
       const int lim = p.causal ? (kv - sq.delta - q0 - 32 * grp) : INT_MIN;
       const bool need_mask = __any_sync(0xffffffffu, !row_ok || lim > 0);
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + (t & 1)), (t >> 1) & 1, wc, 7))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::S + (t & 1)), (t >> 1) & 1, wc, 7))) break;
       tc_fence_after();
       uint32_t pk[16];
       {
@@ -400,10 +446,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           float2 xa = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 0]), __uint_as_float(sr[4 * c4 + 1])), sc2, nl.x));
           float2 xb = f2_split(fma_f32x2(f2_bits(__uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])), sc2, nl.y));
           if constexpr (BIAS) {
-            xa.x = fmaf(bv[c + 0], 1.4426950408889634f, xa.x);
-            xa.y = fmaf(bv[c + 1], 1.4426950408889634f, xa.y);
-            xb.x = fmaf(bv[c + 2], 1.4426950408889634f, xb.x);
-            xb.y = fmaf(bv[c + 3], 1.4426950408889634f, xb.y);
+            float bv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) bv[e] = c + e < bvalid ? half_to_float<BF16>(bcol[(c + e) * bstep]) : 0.f;
+            const uint64_t l2e = f2_bits(1.4426950408889634f, 1.4426950408889634f);
+            xa = f2_split(fma_f32x2(f2_bits(bv[0], bv[1]), l2e, f2_bits(xa.x, xa.y)));
+            xb = f2_split(fma_f32x2(f2_bits(bv[2], bv[3]), l2e, f2_bits(xb.x, xb.y)));
           }
           float e0 = ex2_approx(xa.x);
           float e1 = ex2_approx(xa.y);
@@ -419,12 +467,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           pk[2 * c4 + 1] = pack2<BF16>(e2, e3);
         }
       }
+      if constexpr (BIAS) {
+        __syncwarp();                       // this warp's bias reads are done: release the tile
+        if (lane == 0) mbar_arrive(bar(BR::BEMPTY + (t & (BSTAGES - 1))));
+      }
       tmem_st_x16(tS, pk);                  // P^T, 16-bit, over the columns just read
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P + (t & 1)));
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DP), t & 1, wc, 8))) break;
+      if (lane == 0) mbar_arrive(bar(BR::P + (t & 1)));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::DP), t & 1, wc, 8))) break;
       tc_fence_after();
       uint32_t dk[16];
       {
@@ -433,7 +485,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DPFREE));   // dP^T buffer may now take the next tile's G2
+        if (lane == 0) mbar_arrive(bar(BR::DPFREE));   // dP^T buffer may now take the next tile's G2
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           // dS = P * (dP - D), two columns per instruction
@@ -449,12 +501,43 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       if constexpr (BIAS) {
-        // dBias = dS (the bias enters S with weight 1), the 16-bit values G4 and G5 use
-        if (p.m.dbias != nullptr && row_ok) {
-          uint16_t* dcol = static_cast<uint16_t*>(p.m.dbias) + bias_row(p.m.dbias_st, b, h, qc) + kv;
+        // dBias = dS (the bias enters S with weight 1), the 16-bit values G4 and G5 use.
+        // The group's [32 query x 128 key] block goes through shared memory and one
+        // TMA store (which clips at the tensor's extent).  In a packed batch the
+        // extent is the longest sequence, so a block that crosses this sequence's
+        // end is stored element by element instead (the caller's dBias outside
+        // the sequence is never written).
+        if (p.m.dbias != nullptr && qc < sq.nq) {
+          const bool by_tma = p.m.cu_q == nullptr || (qc + 32 <= sq.nq && kv0 + BN <= sq.nk);
+          if (by_tma) {
+            uint8_t* half = smem + L::OFF_DB + grp * L::DB_HALF;
+            if (n_db > 0) {
+              if (db_lead) {
+                bulk_wait_group_read<0>();                  // the previous block has been read out
+                mbar_arrive(bar(BR::DBFREE + grp));
+              }
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::DBFREE + grp), (n_db - 1) & 1, wc, 18))) break;
+            }
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (qc + c < sq.nq) dcol[c * p.m.dbias_st.n] = static_cast<uint16_t>(dk[c >> 1] >> (16 * (c & 1)));
+            for (int c = 0; c < 32; ++c)
+              *reinterpret_cast<uint16_t*>(half + c * (BN * 2) + r * 2) = static_cast<uint16_t>(dk[c >> 1] >> (16 * (c & 1)));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BR::DBFULL + grp));
+            if ((warp & 3) == 0) {                          // the group's first warp issues the store
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::DBFULL + grp), n_db & 1, wc, 19))) break;
+              if (lane == 0) {
+                tma_store_4d(&tm_dbias, smem_u32(half), kv0, qc, h, b);
+                bulk_commit_group();
+              }
+            }
+            ++n_db;
+          } else if (row_ok) {
+            uint16_t* dcol = static_cast<uint16_t*>(p.m.dbias) + bias_row(p.m.dbias_st, b, h, qc) + kv;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (qc + c < sq.nq) dcol[c * p.m.dbias_st.n] = static_cast<uint16_t>(dk[c >> 1] >> (16 * (c & 1)));
+          }
         }
       }
       {
@@ -462,7 +545,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // (MN-major B): 128 B per row (this group's 64 B are 16-byte chunks
         // 4 grp .. 4 grp + 3), chunk c stored at chunk position c ^ (r mod 8)
         // (the 128-byte swizzle).
-        if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (t - 1) & 1, wc, 9))) break;
+        if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(BR::DSFREE), (t - 1) & 1, wc, 9))) break;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = 4 * grp + i;
@@ -472,8 +555,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DS));
+      if (lane == 0) mbar_arrive(bar(BR::DS));
     }
+    if constexpr (BIAS)
+      if (db_lead && n_db > 0) bulk_wait_group<0>();      // stores complete before the CTA exits
   } else if (warp >= 12) {
     // ================================================================ dQ group
     if constexpr (!DET) {
@@ -483,7 +568,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int h = hkv * G, qi = i0;                          // head and query tile of tile t
       for (int t = 0; t < T; ++t) {
         const int q0 = qi * BM;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), t & 1, wc, 10))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::DQFULL), t & 1, wc, 10))) break;
         tc_fence_after();
         uint32_t v0[32], v1[32];
         tmem_ld_x32(tdQ, v0);
@@ -491,7 +576,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DQEMPTY));
+        if (lane == 0) mbar_arrive(bar(BR::DQEMPTY));
         // Thread r holds column r of the 64 x d tile: for each query row, the 32
         // lanes of a warp add one contiguous 128-byte segment of the accumulator.
         if (r < D) {
@@ -521,7 +606,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                    at(is_dk ? p.m.st.dk : p.m.st.dv, p.m, b, hkv, sq.k_start + kv) * 2;
     bool have = T > 0;
     if (have) {
-      have = __all_sync(0xffffffffu, mbar_wait(bar(B_ACC), 0, wc, 13));
+      have = __all_sync(0xffffffffu, mbar_wait(bar(BR::ACC), 0, wc, 13));
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0;
@@ -553,8 +638,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D, bool BF16, bool DET, bool BIAS>
 cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
-                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  using L = Layout<D>;
+                     const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb, const CUtensorMap& tdb,
+                     cudaStream_t stream) {
+  using L = Layout<D, BIAS>;
   auto kern = bwd_main_kernel<D, BF16, DET, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
@@ -572,32 +658,33 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   p.m = seq_map(a.pb);
   const long long nkt = (a.pb.Nkv + BN - 1) / BN;
   const long long grid = nkt * a.pb.B * a.pb.Hkv;
-  kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, tb, tdb, p);
   return cudaGetLastError();
 }
 
 template <int D, bool BF16, bool DET>
 cudaError_t launch_b(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                     const CUtensorMap& tv, cudaStream_t stream) {
-  return a.pb.bias != nullptr ? launch_t<D, BF16, DET, true>(a, tq, tdo, tk, tv, stream)
-                              : launch_t<D, BF16, DET, false>(a, tq, tdo, tk, tv, stream);
+                     const CUtensorMap& tv, const CUtensorMap& tb, const CUtensorMap& tdb, cudaStream_t stream) {
+  return a.pb.bias != nullptr ? launch_t<D, BF16, DET, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+                              : launch_t<D, BF16, DET, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
-                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
+                            const CUtensorMap& tdb, cudaStream_t stream) {
   const bool det = a.pb.deterministic != 0;
   if (a.pb.d > 64) {
-    if (a.pb.bf16) return det ? launch_b<128, true, true>(a, tq, tdo, tk, tv, stream)
-                              : launch_b<128, true, false>(a, tq, tdo, tk, tv, stream);
-    return det ? launch_b<128, false, true>(a, tq, tdo, tk, tv, stream)
-               : launch_b<128, false, false>(a, tq, tdo, tk, tv, stream);
+    if (a.pb.bf16) return det ? launch_b<128, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+                              : launch_b<128, true, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
+    return det ? launch_b<128, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+               : launch_b<128, false, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
   }
-  if (a.pb.bf16) return det ? launch_b<64, true, true>(a, tq, tdo, tk, tv, stream)
-                            : launch_b<64, true, false>(a, tq, tdo, tk, tv, stream);
-  return det ? launch_b<64, false, true>(a, tq, tdo, tk, tv, stream)
-             : launch_b<64, false, false>(a, tq, tdo, tk, tv, stream);
+  if (a.pb.bf16) return det ? launch_b<64, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+                            : launch_b<64, true, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
+  return det ? launch_b<64, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+             : launch_b<64, false, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
 }
 
 }  // namespace fa

@@ -16,10 +16,14 @@
 // more than 8, which keeps P <= 256 and makes rescaling rare after the first
 // tiles.
 //
-// Warp roles (256 threads): warp 0 TMA producer (Q once, 3-stage K/V ring), warp 1 owns
-// TMEM and issues G1, warp 2 issues PV, warps 4-7 thread r owns query row r
-// (TMEM lane r) and all 128 columns of each S tile.  S is double-buffered in
-// TMEM (S0, S1, O = 2 x 128 + d columns).
+// Warp roles (384 threads): warp 0 TMA producer (both query tiles once, a 2-stage K/V
+// ring they share), warp 1 owns TMEM and issues G1, warp 2 issues PV, and one
+// softmax warpgroup per query tile: thread r owns query row r (TMEM lane r) and all
+// 128 columns of each S tile.  TMEM: S_0, S_1, O_0, O_1.
+// With an additive bias the CTA takes one query tile (256 threads), and the freed
+// shared memory holds a 2-stage ring of [128 query x 128 key] bias tiles that the
+// producer loads by TMA next to K and V (128-byte swizzle, so that each thread
+// reads its own row in 16-byte pieces without bank conflicts).
 #include <cstdint>
 #include <climits>
 #include <math_constants.h>
@@ -32,21 +36,30 @@ namespace fa {
 namespace {
 
 constexpr int BQ = 128;     // query rows per tile (TMEM lanes)
-constexpr int NT = 2;       // query tiles per CTA, one softmax warpgroup each
 constexpr int BK = 128;     // KV rows per step
-constexpr int STAGES = 2;   // K/V ring depth (each K/V tile serves both query tiles)
-constexpr int kThreads = 128 + NT * 128;
+constexpr int STAGES = 2;   // K/V ring depth (each K/V tile serves every query tile of the CTA)
+constexpr int BSTAGES = 2;  // bias ring depth
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 
-template <int D>
+// query tiles per CTA (one softmax warpgroup each) and threads
+template <bool BIAS>
+struct Cfg {
+  static constexpr int NT = BIAS ? 1 : 2;
+  static constexpr int kThreads = 128 + NT * 128;
+};
+
+template <int D, bool BIAS>
 struct Layout {
+  static constexpr int NT = Cfg<BIAS>::NT;
   static constexpr int NH = D / 64;
   static constexpr int HALF = 128 * 128;        // one 64-column half of a 128-row tile
   static constexpr int TILE = NH * HALF;
   static constexpr int OFF_Q = 0;               // query tile x at OFF_Q + x*TILE
   static constexpr int OFF_KV = NT * TILE;      // stage s: K at OFF_KV + 2*s*TILE, V after it
-  static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE;
-  static constexpr int NBAR = 16;
+  static constexpr int OFF_BIAS = OFF_KV + STAGES * 2 * TILE;
+  static constexpr int BIAS_TILE = 2 * HALF;    // [128 query x 128 key], two 64-key halves
+  static constexpr int OFF_BAR = OFF_BIAS + (BIAS ? BSTAGES * BIAS_TILE : 0);
+  static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = (TOTAL + 1024) > 120 * 1024 ? (TOTAL + 1024) : 120 * 1024;
@@ -58,9 +71,9 @@ struct Layout {
 
 enum : int {
   B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_SFREE = B_P + 2,
-  B_PV = B_SFREE + 2, B_AFIN = B_PV + 2, B_END
+  B_PV = B_SFREE + 2, B_AFIN = B_PV + 2, B_BFULL, B_BEMPTY = B_BFULL + BSTAGES, B_END = B_BEMPTY + BSTAGES
 };
-static_assert(B_END <= 16, "barrier count");
+static_assert(B_END <= 24, "barrier count");
 
 struct Params {
   void* o;
@@ -80,10 +93,11 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int D, bool BF16, bool BIAS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BIAS>::kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using L = Layout<D>;
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias, const Params p) {
+  using L = Layout<D, BIAS>;
+  constexpr int NT = L::NT;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled tiles.  Offsetting the array itself
   // (not a rounded integer) keeps the pointer in the shared address space, so
@@ -136,6 +150,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_init(bar(B_PV + x), 1);
     }
     mbar_init(bar(B_AFIN), 1);
+    for (int i = 0; i < BSTAGES; ++i) {
+      mbar_init(bar(B_BFULL + i), 1);
+      mbar_init(bar(B_BEMPTY + i), 4);  // one arrival per softmax warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -172,11 +190,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           tma_load_4d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
           tma_load_4d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
         }
+        if constexpr (BIAS) {
+          // bias of (query rows q0.., keys t*BK..) of head h, sequence b; a broadcast
+          // axis has extent 1 in the map and is addressed at 0
+          const int bs = t & (BSTAGES - 1);
+          if (t >= BSTAGES && !mbar_wait(bar(B_BEMPTY + bs), ((t / BSTAGES) & 1) ^ 1, wc, 59)) break;
+          const uint32_t bb = bar(B_BFULL + bs);
+          mbar_arrive_expect_tx(bb, L::BIAS_TILE);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_4d(sb + L::OFF_BIAS + bs * L::BIAS_TILE + hh * L::HALF, &tm_bias, bb, t * BK + 64 * hh,
+                        p.m.bias_st.n ? q0 : 0, p.m.bias_st.h ? h : 0, p.m.bias_st.b ? b : 0);
+        }
         issued = t + 1;
       }
       drain_wait(bar(B_Q), 0);
       for (int t = max(0, issued - STAGES); t < issued; ++t)
         drain_wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1);
+      if constexpr (BIAS)
+        for (int t = max(0, issued - BSTAGES); t < issued; ++t)
+          drain_wait(bar(B_BFULL + (t & (BSTAGES - 1))), (t / BSTAGES) & 1);
     }
   } else if (warp == 1 || warp == 2) {
     // ================================================================ MMA issuers
@@ -246,8 +279,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t tO = tmem + lane_off + L::COL_O + qt * 128;
     const int q = q0 + qt * BQ + r;
     const int T = Tx[qt];
-    const uint16_t* brow = nullptr;                     // this row of the bias
-    if constexpr (BIAS) brow = static_cast<const uint16_t*>(p.m.bias) + bias_row(p.m.bias_st, b, h, q);
+    // this thread's row of a staged bias tile (row 0 when the bias broadcasts over queries)
+    const int brow = p.m.bias_st.n ? r : 0;
     float m_ref = -CUDART_INF_F;                        // reference max (log2 units); -inf: no key seen yet
     const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
     float l = 0.f;                                      // sum of 2^(x - m_ref)
@@ -263,29 +296,35 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tc_fence_after();
       float x[BK];
       if constexpr (BIAS) {
+        const int bs = t & (BSTAGES - 1);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_BFULL + bs), (t / BSTAGES) & 1, wc, 60))) { ok = false; break; }
+        const uint8_t* btile = smem + L::OFF_BIAS + bs * L::BIAS_TILE + brow * 128;
 #pragma unroll
         for (int ch = 0; ch < BK / 32; ++ch) {
           uint32_t sr[32];
           tmem_ld_x32(tS + 32 * ch, sr);
-          // x = S * scale * log2(e) + bias * log2(e)
+          // x = S * scale * log2(e) + bias * log2(e); keys 32 ch .. 32 ch + 31 are 16-byte
+          // chunks 4 ch .. 4 ch + 3 of the row, chunk k of a 128-byte half stored at k ^ (row mod 8)
           float bv[32];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            float v8[8];
-            if (q < sq.nq) {
-              bias8<BF16>(brow, kv0 + 32 * ch + 8 * j, sq.nk, v8);
-            } else {
+            const int k = 4 * ch + j;
+            const uint4 u = *reinterpret_cast<const uint4*>(btile + (k >> 3) * L::HALF + (((k & 7) ^ (brow & 7)) << 4));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = unpack2<BF16>(w[e]);
+              bv[8 * j + 2 * e] = q < sq.nq ? f.x : 0.f;
+              bv[8 * j + 2 * e + 1] = q < sq.nq ? f.y : 0.f;
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) bv[8 * j + e] = v8[e];
           }
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             x[32 * ch + c] = fmaf(bv[c], 1.4426950408889634f, __uint_as_float(sr[c]) * p.scale_log2);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_BEMPTY + bs));   // this warp's bias reads are done
       } else {
         // all four 32-column loads in flight at once, one wait
         uint32_t sr[BK];
@@ -407,8 +446,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 template <int D, bool BF16, bool BIAS>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     unsigned int* status, cudaStream_t stream) {
-  using L = Layout<D>;
+                     const CUtensorMap& tb, unsigned int* status, cudaStream_t stream) {
+  using L = Layout<D, BIAS>;
+  constexpr int NT = L::NT;
   auto kern = fwd_kernel<D, BF16, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
@@ -421,27 +461,27 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.causal = a.pb.causal;
   p.m = seq_map(a.pb);
   const long long grid = static_cast<long long>(((a.pb.Nq + BQ - 1) / BQ + NT - 1) / NT) * a.pb.B * a.pb.Hq;
-  kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
+  kern<<<static_cast<unsigned>(grid), Cfg<BIAS>::kThreads, L::ALLOC, stream>>>(tq, tk, tv, tb, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       unsigned int* status, cudaStream_t stream) {
+                       const CUtensorMap& tb, unsigned int* status, cudaStream_t stream) {
   const bool bias = a.pb.bias != nullptr;
   if (a.pb.d > 64) {
     if (a.pb.bf16)
-      return bias ? launch_t<128, true, true>(a, tq, tk, tv, status, stream)
-                  : launch_t<128, true, false>(a, tq, tk, tv, status, stream);
-    return bias ? launch_t<128, false, true>(a, tq, tk, tv, status, stream)
-                : launch_t<128, false, false>(a, tq, tk, tv, status, stream);
+      return bias ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, stream)
+                  : launch_t<128, true, false>(a, tq, tk, tv, tb, status, stream);
+    return bias ? launch_t<128, false, true>(a, tq, tk, tv, tb, status, stream)
+                : launch_t<128, false, false>(a, tq, tk, tv, tb, status, stream);
   }
   if (a.pb.bf16)
-    return bias ? launch_t<64, true, true>(a, tq, tk, tv, status, stream)
-                : launch_t<64, true, false>(a, tq, tk, tv, status, stream);
-  return bias ? launch_t<64, false, true>(a, tq, tk, tv, status, stream)
-              : launch_t<64, false, false>(a, tq, tk, tv, status, stream);
+    return bias ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, stream)
+                : launch_t<64, true, false>(a, tq, tk, tv, tb, status, stream);
+  return bias ? launch_t<64, false, true>(a, tq, tk, tv, tb, status, stream)
+              : launch_t<64, false, false>(a, tq, tk, tv, tb, status, stream);
 }
 
 }  // namespace fa

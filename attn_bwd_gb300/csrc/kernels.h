@@ -122,16 +122,20 @@ cudaError_t launch_wait_selftest(unsigned int* status, long long timeout_ns, cud
 // Writes dBias = 0 where the main kernel, under causal tile skipping, never visits.
 cudaError_t launch_dbias_zero(const Problem& pb, unsigned int* status, cudaStream_t stream);
 
-// bwd_main.cu: maps are Q, dO (box 64 x 64 rows), K, V (box 64 x 128 rows)
+// bwd_main.cu: maps are Q, dO (box 64 x 64 rows), K, V (box 64 x 128 rows), the bias
+// (box 128 keys x 64 queries) and dBias (box 128 keys x 32 queries); the last two are
+// used only when the problem has a bias (and a dBias)
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
-                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
+                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
+                            const CUtensorMap& tdb, cudaStream_t stream);
 
 // bwd_dq.cu: maps are Q, dO (box 64 x 128 rows), K, V (box 64 x 128 rows)
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
-// fwd.cu: maps are Q, K, V (box 64 x 128 rows)
+// fwd.cu: maps are Q, K, V (box 64 x 128 rows) and the bias (box 64 keys x 128 queries,
+// 128-byte swizzle; used only when the problem has a bias)
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       unsigned int* status, cudaStream_t stream);
+                       const CUtensorMap& tb, unsigned int* status, cudaStream_t stream);
 
 }  // namespace fa

@@ -73,3 +73,52 @@ def test_bias_with_gqa_and_head_dim_128():
     g = torch.Generator().manual_seed(74)
     bias = torch.randn(1, 8, 257, 128, generator=g).to(torch.bfloat16)
     _run(shape, bias, 75, False)
+
+
+@pytest.mark.parametrize("det", [False, True])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_bias_on_packed_batch(causal, det):
+    """A per-sequence bias on a packed batch: [B, Hq, max_q, >= max_k] with a padded key axis.
+    Sequence b reads and writes only rows [0, nq_b) x keys [0, nk_b) of its bias and dBias;
+    the rest of the caller's dBias keeps its sentinel.  Lengths make some blocks lie inside a
+    sequence and others cross its end in queries, keys or both."""
+    lens_q, lens_k, Hq, Hkv, d = (77, 300, 16, 129), (200, 130, 16, 257), 4, 2, 128
+    pk = inputs.Packed(lens_q, lens_k, Hq, Hkv, d, causal, "bf16")
+    q, k, v, do = inputs.draw_packed(pk, 76)
+    B, mq, mk, kpad = len(lens_q), max(lens_q), max(lens_k), 264     # key axis padded to a multiple of 8
+    g = torch.Generator().manual_seed(77)
+    bias = (1.5 * torch.randn(B, Hq, mq, kpad, generator=g)).to(torch.bfloat16)
+    cu_q, cu_k = pk.cu_q, pk.cu_k
+    qd, kd, vd, dod, bd = (t.cuda() for t in (q, k, v, do, bias))
+    cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+    ck = torch.tensor(cu_k, dtype=torch.int32, device="cuda")
+    st_b = (Hq * mq * kpad, mq * kpad, kpad)
+    o, lse = torch.empty_like(qd), torch.empty(Hq, cu_q[-1], dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    assert _lib.fa_fwd_bias(qd, kd, vd, o, lse, _lib.make_bias(bd, st_b), None, cq, ck, B, Hq, Hkv, mq, mk,
+                            cu_q[-1], cu_k[-1], d, pk.softmax_scale, causal, _lib.FA_BF16, s) == _lib.FA_OK
+    sentinel = 7.0
+    db = torch.full((B, Hq, mq, kpad), sentinel, dtype=torch.bfloat16, device="cuda")
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    n = _lib.fa_bwd_varlen_workspace_size(B, Hq, Hkv, mq, mk, d, int(det))
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    assert _lib.fa_bwd_bias(qd, kd, vd, o, dod, lse, dq, dk, dv, _lib.make_bias(bd, st_b, db, st_b), None, cq, ck, B,
+                            Hq, Hkv, mq, mk, cu_q[-1], cu_k[-1], d, pk.softmax_scale, causal, _lib.FA_BF16, int(det),
+                            ws, n, s) == _lib.FA_OK
+    torch.cuda.synchronize()
+    assert _lib.fa_last_device_error() == _lib.FA_OK
+    dbh = db.cpu()
+    untouched = torch.ones(B, Hq, mq, kpad, dtype=torch.bool)
+    for b in range(B):
+        nq, nk = lens_q[b], lens_k[b]
+        untouched[b, :, :nq, :nk] = False
+        sl_q, sl_k = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        qb, kb, vb, dob = (t[:, sl][None] for t, sl in ((q, sl_q), (k, sl_k), (v, sl_k), (do, sl_q)))
+        bb = bias[b:b + 1, :, :nq, :nk]
+        o_ref, l_ref = attn_ref.forward(qb, kb, vb, pk.softmax_scale, causal, bias=bb)
+        r = attn_ref.backward(qb, kb, vb, dob, pk.softmax_scale, causal, bias=bb)
+        _check({f"O[{b}]": (_np(o[:, sl_q][None]), o_ref), f"L[{b}]": (_np(lse[:, sl_q][None]), l_ref),
+                f"dQ[{b}]": (_np(dq[:, sl_q][None]), r["dq"]), f"dK[{b}]": (_np(dk[:, sl_k][None]), r["dk"]),
+                f"dV[{b}]": (_np(dv[:, sl_k][None]), r["dv"]),
+                f"dBias[{b}]": (_np(dbh[b:b + 1, :, :nq, :nk]), r["dbias"])})
+    assert (dbh[untouched] == sentinel).all(), "dBias written outside a sequence"
