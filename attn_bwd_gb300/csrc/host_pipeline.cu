@@ -21,6 +21,7 @@
 // (fa_bwd_host_staging_size); the only state kept here is the copy and slot
 // streams of each device, created on first use.  Every copy is one
 // cudaMemcpyAsync of a contiguous range.
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -50,7 +51,13 @@ int device_streams(Streams* out) {
               cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking) == cudaSuccess;
     for (int i = 0; ok && i < FA_HOST_MAX_SLOTS; ++i)
       ok = cudaStreamCreateWithFlags(&n.slot[i], cudaStreamNonBlocking) == cudaSuccess;
-    if (!ok) return FA_ERR_CUDA;   // (a failed creation leaves the device without cached streams)
+    if (!ok) {   // release what was created; the next call tries again
+      for (cudaStream_t x : {n.in, n.out})
+        if (x) cudaStreamDestroy(x);
+      for (cudaStream_t x : n.slot)
+        if (x) cudaStreamDestroy(x);
+      return FA_ERR_CUDA;
+    }
     s = n;
   }
   *out = s;
@@ -147,6 +154,10 @@ int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, cons
   }
   if (staging == nullptr || staging_bytes < need) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(staging) & (kAlign - 1)) != 0) return FA_ERR_ALIGN;
+  // the remaining arguments fa_bwd checks, checked before any copy is queued (so that a
+  // rejected call leaves nothing in flight)
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
   Streams ss;
   int st = device_streams(&ss);
   if (st) return st;

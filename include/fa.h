@@ -345,7 +345,11 @@ int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, cons
  * chunk_groups in [1, B*Hkv], slots in [1, FA_HOST_MAX_SLOTS] (FA_ERR_SHAPE
  * otherwise).  staging: >= fa_bwd_host_staging_size(...) bytes (0 for invalid
  * arguments), 256-byte aligned (FA_ERR_ALIGN), not used by anything else until
- * `stream` passes the call (FA_ERR_WORKSPACE if NULL or too small).
+ * `stream` passes the call (FA_ERR_WORKSPACE if NULL or too small).  Every
+ * argument error (shape, dtype, scale, causal, staging) is returned before
+ * anything is queued; only FA_ERR_CUDA from a failed copy or launch can leave
+ * earlier chunks' work in flight (synchronise the device before reusing the
+ * buffers then).
  */
 #define FA_HOST_MAX_SLOTS 8
 

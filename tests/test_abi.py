@@ -239,3 +239,8 @@ def test_host_pipeline_validation_and_staging_size(lib):
     assert _lib.fa_bwd_host(*args, 2, 2, W + 16, 1 << 30) == _lib.FA_ERR_ALIGN
     bad = [A] * 9 + [5, 4, 3, 100, 100, 64, 0.1, 1, _lib.FA_BF16, 0]
     assert _lib.fa_bwd_host(*bad, 1, 2, W, 1 << 30) == _lib.FA_ERR_GQA
+    # dtype, scale and causal are rejected before any copy is queued (no CUDA call is made)
+    base = [A] * 9 + [5, 4, 2, 100, 100, 64]
+    assert _lib.fa_bwd_host(*base, 0.1, 1, 7, 0, 2, 2, W, 1 << 30) == _lib.FA_ERR_DTYPE
+    assert _lib.fa_bwd_host(*base, float("nan"), 1, _lib.FA_BF16, 0, 2, 2, W, 1 << 30) == _lib.FA_ERR_ARG
+    assert _lib.fa_bwd_host(*base, 0.1, 3, _lib.FA_BF16, 0, 2, 2, W, 1 << 30) == _lib.FA_ERR_ARG
