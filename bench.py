@@ -170,22 +170,40 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(pw) if pw else None}
 
 
-def run_cpu_baseline(sh, heads=4):
-    """The fp64 oracle, as it stands, on one (batch, kv-head) group of the workload."""
+def group_parity(grads, ref) -> dict:
+    """max|gpu - oracle| / (1e-2 max|oracle| + 1e-3) per tensor (<= 1 passes), for the GPU's
+    (dq, dk, dv) of one group against the oracle's dict of fp64 arrays."""
+    import numpy as np
+    out = {}
+    for name, got in zip(("dq", "dk", "dv"), grads):
+        g = got.detach().cpu().double().numpy()
+        r = ref[name]
+        out[name] = float(np.abs(g - r).max()) / (1e-2 * float(np.abs(r).max()) + 1e-3)
+    return out
+
+
+def run_cpu_baseline(sh, group=None):
+    """The fp64 oracle, as it stands, on one (batch, kv-head) group of the workload (all of its
+    query heads).  `group` = (q, k, v, do, dq, dk, dv) of that group as the GPU saw and produced
+    them (batch 0, kv head 0): the oracle then runs on those inputs, and the GPU's gradients are
+    compared with its result.  Returns (baseline, parity or None)."""
     from attn_bwd_gb300 import inputs
     from oracle import attn_ref
     G = sh.Hq // sh.Hkv
-    sub = inputs.Shape(1, G, 1, sh.Nq, sh.Nkv, sh.d, sh.causal, sh.dtype)
-    q, k, v, do = inputs.draw(sub, 12345)
-    q, do = q[:, :heads], do[:, :heads]
+    if group is None:
+        sub = inputs.Shape(1, G, 1, sh.Nq, sh.Nkv, sh.d, sh.causal, sh.dtype)
+        q, k, v, do = inputs.draw(sub, 12345)
+    else:
+        q, k, v, do = group[:4]
     t0 = time.perf_counter()
-    attn_ref.backward(q, k, v, do, sh.softmax_scale, sh.causal)
+    ref = attn_ref.backward(q, k, v, do, sh.softmax_scale, sh.causal)
     dt = time.perf_counter() - t0
-    f = 10.0 * heads * sh.Nq * sh.Nkv * sh.d / (2 if sh.causal else 1)
+    f = 10.0 * G * sh.Nq * sh.Nkv * sh.d / (2 if sh.causal else 1)
     cores = len(os.sched_getaffinity(0))
-    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} query heads of one (batch, kv-head) group at Nq=Nkv={sh.Nq}, "
+    base = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{G} query heads of one (batch, kv-head) group at Nq=Nkv={sh.Nq}, "
                       f"fp64 numpy/OpenBLAS, {dt:.1f} s wall"}
+    return base, (group_parity(group[4:], ref) if group is not None else None)
 
 
 def reference_arm(args):
@@ -424,7 +442,18 @@ def main():
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = run_cpu_baseline(sh)
+        # the oracle on batch 0 / kv head 0 of this run's own inputs; the same run's gradients of
+        # that group are checked against it (the last timed step wrote dq, dk, dv)
+        G = Hq // Hkv
+        grp = tuple(t[0:1, 0:n].cpu() for t, n in ((q, G), (k, 1), (v, 1), (do, G), (dq, G), (dk, 1), (dv, 1)))
+        try:
+            base, par = run_cpu_baseline(sh, grp)
+            line["cpu_baseline"] = base
+            line["parity"] = dict(par, group="batch 0, kv head 0 with its query heads, full length",
+                                  bound="max|gpu - oracle| / (1e-2 max|oracle| + 1e-3), <= 1 passes")
+        except Exception as e:   # the measurement line is printed whatever happens here
+            line["cpu_baseline"], _ = run_cpu_baseline(sh)
+            line["parity"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -36,3 +36,34 @@ def test_reference_arm_other_ranks_are_silent():
     r = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_bench_parity_of_one_group():
+    """The bench's CPU leg runs the oracle on one group of the run's own inputs and reports the
+    GPU gradients' error against it; here the 'GPU' gradients are the oracle's own (rounded to
+    16 bits), then one with a planted error."""
+    import torch
+    from attn_bwd_gb300 import inputs
+    from oracle import attn_ref
+    bench = _bench_module()
+    sh = inputs.Shape(1, 4, 1, 96, 96, 32, 1, "bf16")
+    q, k, v, do = inputs.draw(sh, 5)
+    ref = attn_ref.backward(q, k, v, do, sh.softmax_scale, sh.causal)
+    grads = [torch.from_numpy(ref[n]).to(torch.bfloat16) for n in ("dq", "dk", "dv")]
+    base, par = bench.run_cpu_baseline(sh, (q, k, v, do, *grads))
+    assert base["kind"] == "oracle" and base["value"] > 0 and base["cores"] >= 1
+    assert set(par) == {"dq", "dk", "dv"} and all(0 <= r < 0.5 for r in par.values()), par
+    bad = grads[0].clone()
+    bad[0, 1, 7, 3] += 0.05 * float(bad.float().abs().max())
+    _, par2 = bench.run_cpu_baseline(sh, (q, k, v, do, bad, grads[1], grads[2]))
+    assert par2["dq"] > 1.0 and par2["dk"] == par["dk"]
+    base3, none = bench.run_cpu_baseline(sh)
+    assert none is None and base3["value"] > 0
