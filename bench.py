@@ -445,8 +445,8 @@ def main():
         # the oracle on batch 0 / kv head 0 of this run's own inputs; the same run's gradients of
         # that group are checked against it (the last timed step wrote dq, dk, dv)
         G = Hq // Hkv
-        grp = tuple(t[0:1, 0:n].cpu() for t, n in ((q, G), (k, 1), (v, 1), (do, G), (dq, G), (dk, 1), (dv, 1)))
         try:
+            grp = tuple(t[0:1, 0:n].cpu() for t, n in ((q, G), (k, 1), (v, 1), (do, G), (dq, G), (dk, 1), (dv, 1)))
             base, par = run_cpu_baseline(sh, grp)
             line["cpu_baseline"] = base
             line["parity"] = dict(par, group="batch 0, kv head 0 with its query heads, full length",
