@@ -16,11 +16,20 @@
 namespace fa {
 namespace {
 
-// Device status word shared by every kernel family (first failure wins).
+// Device-wide report word shared by every kernel (first failure since the last
+// fa_last_device_error() wins).  Kernels only write it; none acts on it.
 __device__ unsigned int g_status;
+
+// Abort words of forward calls (a backward call keeps its own in its workspace).
+// Each fa_fwd* call takes the next slot and zeroes it on its stream before the
+// launch, so calls in flight at the same time (up to kFwdSlots) never share one.
+constexpr int kFwdSlots = 256;
+__device__ unsigned int g_fwd_abort[kFwdSlots];
 
 constexpr int kMaxDevices = 64;
 unsigned int* g_status_ptr[kMaxDevices] = {};
+unsigned int* g_fwd_abort_ptr[kMaxDevices] = {};
+unsigned int g_fwd_next[kMaxDevices] = {};
 std::mutex g_mu;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -38,6 +47,20 @@ int status_ptr(unsigned int** out) {
     g_status_ptr[dev] = static_cast<unsigned int*>(p);
   }
   *out = g_status_ptr[dev];
+  return FA_OK;
+}
+
+// Next forward abort slot of the current device.
+int fwd_abort_slot(unsigned int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_fwd_abort_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_abort) != cudaSuccess) return FA_ERR_CUDA;
+    g_fwd_abort_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_fwd_abort_ptr[dev] + (g_fwd_next[dev]++ % kFwdSlots);
   return FA_OK;
 }
 
@@ -119,9 +142,10 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // The fp32 dQ accumulator rows are as wide as the kernel that fills them (64 or 128).
 int kernel_d(int d) { return d <= 64 ? 64 : 128; }
 
+// Workspace: [256 B: the call's abort word][-L*log2e][D][fp32 dQ accumulator (atomic mode)].
 size_t ws_bytes(int B, int Hq, int Nq, int d, int deterministic) {
   const size_t rows = static_cast<size_t>(B) * Hq * round_up(Nq, kRowPad);
-  size_t total = 2 * align_up(rows * sizeof(float));
+  size_t total = kAlign + 2 * align_up(rows * sizeof(float));
   if (!deterministic) total += align_up(rows * kernel_d(d) * sizeof(float));
   return total;
 }
@@ -130,6 +154,8 @@ Workspace carve(void* ws, int B, int Hq, int Nq, int d, int deterministic) {
   const size_t rows = static_cast<size_t>(B) * Hq * round_up(Nq, kRowPad);
   uint8_t* p = static_cast<uint8_t*>(ws);
   Workspace w;
+  w.abort = reinterpret_cast<unsigned int*>(p);
+  p += kAlign;
   w.nLg = reinterpret_cast<float*>(p);
   w.Dv = reinterpret_cast<float*>(p + align_up(rows * sizeof(float)));
   w.dq_acc = deterministic ? nullptr : reinterpret_cast<float*>(p + 2 * align_up(rows * sizeof(float)));
@@ -273,6 +299,8 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   if ((st = get_encoder())) return st;
   unsigned int* status = nullptr;
   if ((st = status_ptr(&status))) return st;
+  unsigned int* call_abort = nullptr;
+  if ((st = fwd_abort_slot(&call_abort))) return st;
   CUtensorMap tq, tk, tv;
   const int bf = a.pb.bf16;
   if ((st = map_q(&tq, q, g.st.q, bf, g, 128))) return st;
@@ -281,7 +309,8 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   CUtensorMap tb{};
   if (g.bias != nullptr && (st = make_bias_map(&tb, g.bias, bf, g.Nkv, g.Nq, g.Hq, g.B, g.bias_st, 64, 128)))
     return st;
-  return cuda_status(launch_fwd(a, tq, tk, tv, tb, status, stream));
+  if ((st = cuda_status(cudaMemsetAsync(call_abort, 0, sizeof(unsigned int), stream)))) return st;
+  return cuda_status(launch_fwd(a, tq, tk, tv, tb, status, call_abort, stream));
 }
 
 int run_preprocess(const Geo& g, const void* o, const void* dO, const float* lse, int dtype, int deterministic,

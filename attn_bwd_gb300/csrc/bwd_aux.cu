@@ -24,8 +24,6 @@
 namespace fa {
 namespace {
 
-constexpr int kSMs = 152;
-
 template <bool BF16>
 __device__ __forceinline__ void widen8(const uint4& u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -42,10 +40,12 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
                   float* __restrict__ nLg, float* __restrict__ Dv, float4* __restrict__ dq_acc,
-                  long long rows, int NqPad, SeqMap m, unsigned int* status) {
+                  long long rows, int NqPad, SeqMap m, unsigned int* status, unsigned int* call_abort) {
   constexpr int TPR = D / 8;                 // lanes per row
   constexpr int RPB = 256 / TPR;             // rows per block per sweep
   const int sub = threadIdx.x % TPR;
+  // the later kernels of this call start with a clear abort word
+  if (blockIdx.x == 0 && threadIdx.x == 0) *call_abort = 0u;
   // The sweep base is block-uniform so every lane reaches the row shuffle below.
   for (long long base = static_cast<long long>(blockIdx.x) * RPB; base < rows;
        base += static_cast<long long>(gridDim.x) * RPB) {
@@ -169,9 +169,17 @@ dbias_zero_kernel(SeqMap m, long long rows, unsigned int* status) {
   }
 }
 
+// SM count of the current device (the grid-stride kernels launch up to 16 blocks per SM).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
 long long grid_for(long long work_items, int per_block) {
   long long g = (work_items + per_block - 1) / per_block;
-  const long long cap = static_cast<long long>(kSMs) * 16;
+  const long long cap = static_cast<long long>(sm_count()) * 16;
   if (g > cap) g = cap;
   return g < 1 ? 1 : g;
 }
@@ -183,7 +191,8 @@ cudaError_t pre_t(const Problem& pb, const void* o, const void* dO, const float*
   const long long grid = grid_for(rows, 256 / (D / 8));
   preprocess_kernel<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
       static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws.nLg, ws.Dv,
-      pb.deterministic ? nullptr : reinterpret_cast<float4*>(ws.dq_acc), rows, pb.NqPad, seq_map(pb), status);
+      pb.deterministic ? nullptr : reinterpret_cast<float4*>(ws.dq_acc), rows, pb.NqPad, seq_map(pb), status,
+      ws.abort);
   return cudaGetLastError();
 }
 

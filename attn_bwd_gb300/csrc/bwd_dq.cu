@@ -72,7 +72,8 @@ struct Params {
   const float* nLg;
   const float* Dv;
   void* dq;
-  unsigned int* status;
+  unsigned int* status;       // device-wide report word
+  unsigned int* call_abort;   // this call's abort word (in the workspace)
   SeqMap m;
   int B, Hq, Hkv, Nq, Nkv, NqPad;   // Nq, Nkv: the longest lengths of a packed batch
   float scale, scale_log2;
@@ -151,7 +152,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{p.status, abort_flag};
+  const WaitCtx wc{p.status, p.call_abort, abort_flag};
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -379,6 +380,7 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
   p.Dv = a.ws.Dv;
   p.dq = a.dq;
   p.status = a.status;
+  p.call_abort = a.ws.abort;
   p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv; p.NqPad = a.pb.NqPad;
   p.scale = a.pb.scale;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;

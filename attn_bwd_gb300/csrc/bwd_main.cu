@@ -117,7 +117,8 @@ struct Params {
   float* dq_acc;
   void* dk;
   void* dv;
-  unsigned int* status;
+  unsigned int* status;       // device-wide report word
+  unsigned int* call_abort;   // this call's abort word (in the workspace)
   SeqMap m;
   int B, Hq, Hkv, Nq, Nkv, NqPad;   // Nq, Nkv: the longest lengths of a packed batch
   float scale, scale_log2;
@@ -231,7 +232,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{p.status, abort_flag};
+  const WaitCtx wc{p.status, p.call_abort, abort_flag};
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -651,6 +652,7 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   p.dk = a.dk;
   p.dv = a.dv;
   p.status = a.status;
+  p.call_abort = a.ws.abort;
   p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv; p.NqPad = a.pb.NqPad;
   p.scale = a.pb.scale;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;

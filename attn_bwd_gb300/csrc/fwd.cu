@@ -78,7 +78,8 @@ static_assert(B_END <= 24, "barrier count");
 struct Params {
   void* o;
   float* lse;
-  unsigned int* status;
+  unsigned int* status;       // device-wide report word
+  unsigned int* call_abort;   // this call's abort word
   SeqMap m;
   int B, Hq, Hkv, Nq, Nkv;   // Nq, Nkv: the longest lengths of a packed batch
   float scale_log2;
@@ -165,7 +166,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{p.status, abort_flag};
+  const WaitCtx wc{p.status, p.call_abort, abort_flag};
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -446,7 +447,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 template <int D, bool BF16, bool BIAS>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const CUtensorMap& tb, unsigned int* status, cudaStream_t stream) {
+                     const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort, cudaStream_t stream) {
   using L = Layout<D, BIAS>;
   constexpr int NT = L::NT;
   auto kern = fwd_kernel<D, BF16, BIAS>;
@@ -456,6 +457,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.o = a.o;
   p.lse = a.lse;
   p.status = status;
+  p.call_abort = call_abort;
   p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
@@ -468,20 +470,21 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tb, unsigned int* status, cudaStream_t stream) {
+                       const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort,
+                       cudaStream_t stream) {
   const bool bias = a.pb.bias != nullptr;
   if (a.pb.d > 64) {
     if (a.pb.bf16)
-      return bias ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, stream)
-                  : launch_t<128, true, false>(a, tq, tk, tv, tb, status, stream);
-    return bias ? launch_t<128, false, true>(a, tq, tk, tv, tb, status, stream)
-                : launch_t<128, false, false>(a, tq, tk, tv, tb, status, stream);
+      return bias ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, call_abort, stream)
+                  : launch_t<128, true, false>(a, tq, tk, tv, tb, status, call_abort, stream);
+    return bias ? launch_t<128, false, true>(a, tq, tk, tv, tb, status, call_abort, stream)
+                : launch_t<128, false, false>(a, tq, tk, tv, tb, status, call_abort, stream);
   }
   if (a.pb.bf16)
-    return bias ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, stream)
-                : launch_t<64, true, false>(a, tq, tk, tv, tb, status, stream);
-  return bias ? launch_t<64, false, true>(a, tq, tk, tv, tb, status, stream)
-              : launch_t<64, false, false>(a, tq, tk, tv, tb, status, stream);
+    return bias ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, call_abort, stream)
+                : launch_t<64, true, false>(a, tq, tk, tv, tb, status, call_abort, stream);
+  return bias ? launch_t<64, false, true>(a, tq, tk, tv, tb, status, call_abort, stream)
+              : launch_t<64, false, false>(a, tq, tk, tv, tb, status, call_abort, stream);
 }
 
 }  // namespace fa

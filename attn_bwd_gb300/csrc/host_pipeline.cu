@@ -172,6 +172,14 @@ int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, cons
   const size_t k_grp = static_cast<size_t>(Nkv) * d * 2;
   const size_t l_grp = static_cast<size_t>(G) * Nq * 4;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // After a failure, wait for whatever was queued on the internal streams, so that
+  // no copy into or out of the caller's buffers outlives the call.
+  auto fail = [&](int code) {
+    cudaStreamSynchronize(ss.in);
+    for (int i = 0; i < nslots; ++i) cudaStreamSynchronize(ss.slot[i]);
+    cudaStreamSynchronize(ss.out);
+    return code;
+  };
   // everything starts after whatever the caller queued before (e.g. an earlier use of the staging)
   if (!ok(cudaEventRecord(ev.entry(), stream)) || !ok(cudaStreamWaitEvent(ss.in, ev.entry(), 0))) return FA_ERR_CUDA;
   for (int c = 0; c < nchunks; ++c) {
@@ -182,7 +190,7 @@ int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, cons
     uint8_t* base = at(staging, s * full.bytes);
     const size_t qn = cg * q_grp, kn = cg * k_grp, ln = cg * l_grp;
     // inputs of chunk c, once the slot's previous chunk has been copied out
-    if (c >= nslots && !ok(cudaStreamWaitEvent(ss.in, freed, 0))) return FA_ERR_CUDA;
+    if (c >= nslots && !ok(cudaStreamWaitEvent(ss.in, freed, 0))) return fail(FA_ERR_CUDA);
     if (!ok(cudaMemcpyAsync(base + full.q, at(q, g0 * q_grp), qn, cudaMemcpyHostToDevice, ss.in)) ||
         !ok(cudaMemcpyAsync(base + full.k, at(k, g0 * k_grp), kn, cudaMemcpyHostToDevice, ss.in)) ||
         !ok(cudaMemcpyAsync(base + full.v, at(v, g0 * k_grp), kn, cudaMemcpyHostToDevice, ss.in)) ||
@@ -190,26 +198,26 @@ int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, cons
         !ok(cudaMemcpyAsync(base + full.dO, at(dO, g0 * q_grp), qn, cudaMemcpyHostToDevice, ss.in)) ||
         !ok(cudaMemcpyAsync(base + full.lse, at(lse, g0 * l_grp), ln, cudaMemcpyHostToDevice, ss.in)) ||
         !ok(cudaEventRecord(in_done, ss.in)))
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
     // compute chunk c on its slot's stream
     cudaStream_t cs = ss.slot[s];
-    if (!ok(cudaStreamWaitEvent(cs, in_done, 0))) return FA_ERR_CUDA;
+    if (!ok(cudaStreamWaitEvent(cs, in_done, 0))) return fail(FA_ERR_CUDA);
     st = fa_bwd(base + full.q, base + full.k, base + full.v, base + full.o, base + full.dO,
                 reinterpret_cast<const float*>(base + full.lse), base + full.dq, base + full.dk, base + full.dv, 1,
                 cg * G, cg, Nq, Nkv, d, scale, causal, dtype, deterministic, base + full.ws, full.ws_bytes, cs);
-    if (st) return st;
-    if (!ok(cudaEventRecord(computed, cs))) return FA_ERR_CUDA;
+    if (st) return fail(st);
+    if (!ok(cudaEventRecord(computed, cs))) return fail(FA_ERR_CUDA);
     // outputs of chunk c
     if (!ok(cudaStreamWaitEvent(ss.out, computed, 0)) ||
         !ok(cudaMemcpyAsync(at(dk, g0 * k_grp), base + full.dk, kn, cudaMemcpyDeviceToHost, ss.out)) ||
         !ok(cudaMemcpyAsync(at(dv, g0 * k_grp), base + full.dv, kn, cudaMemcpyDeviceToHost, ss.out)) ||
         !ok(cudaMemcpyAsync(at(dq, g0 * q_grp), base + full.dq, qn, cudaMemcpyDeviceToHost, ss.out)) ||
         !ok(cudaEventRecord(freed, ss.out)))
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
   }
   // the call completes on `stream` once the last outputs are in host memory (the copy-out
   // stream is in order, so its last event covers every chunk)
-  if (!ok(cudaStreamWaitEvent(stream, ev.e[3 * ((nchunks - 1) % nslots) + 2], 0))) return FA_ERR_CUDA;
+  if (!ok(cudaStreamWaitEvent(stream, ev.e[3 * ((nchunks - 1) % nslots) + 2], 0))) return fail(FA_ERR_CUDA);
   return FA_OK;
 }
 

@@ -21,6 +21,8 @@ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Workspace carve-up shared by every stage of the backward.
 struct Workspace {
+  unsigned int* abort;   // the call's abort word (first 256 bytes): zeroed by the preprocess
+                         // kernel, set by the first CTA of the main or dQ kernel that gives up
   float* nLg;     // [B*Hq*NqPad]   -L * log2(e); -inf on padding rows
   float* Dv;      // [B*Hq*NqPad]   rowsum(dO o O); 0 on padding rows
   float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
@@ -135,7 +137,9 @@ cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUte
 
 // fwd.cu: maps are Q, K, V (box 64 x 128 rows) and the bias (box 64 keys x 128 queries,
 // 128-byte swizzle; used only when the problem has a bias)
+// `call_abort` is the call's abort word, zeroed on the stream before the launch.
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tb, unsigned int* status, cudaStream_t stream);
+                       const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort,
+                       cudaStream_t stream);
 
 }  // namespace fa

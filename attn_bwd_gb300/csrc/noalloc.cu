@@ -14,6 +14,7 @@
 // the array's name as an address (on the host it names a stand-in, not device
 // memory): the first call on each device asks the runtime for the device
 // address with that device current, checks the result, and caches it.
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -57,12 +58,15 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic,
                   nullptr, 0, stream);
   }
+  // the checks fa_bwd makes before its workspace check come first here too
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_ARG;
   if (need > FA_STATIC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   void* ws = nullptr;
   const int st = static_scratch(&ws);
   if (st != FA_OK) return st;
-  // Every stage rewrites what it later reads (-L*log2e, D, and the zeroed dQ
-  // accumulator), so whatever an earlier call left in the array is irrelevant.
+  // Every stage rewrites what it later reads (the abort word, -L*log2e, D and the
+  // zeroed dQ accumulator), so whatever an earlier call left in the array is irrelevant.
   return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale, causal, dtype, deterministic, ws,
                 FA_STATIC_SCRATCH_BYTES, stream);
 }

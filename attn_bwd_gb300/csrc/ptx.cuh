@@ -14,8 +14,9 @@
 namespace fa {
 
 // Bound on any single device-side wait.  A wait that runs out records
-// FA_ERR_DEVICE_TIMEOUT (9) in the status word, raises the CTA's abort flag,
-// and the kernel winds down without touching the GPU's health.
+// FA_ERR_DEVICE_TIMEOUT (9) in the device-wide status word, raises its call's
+// abort word and its CTA's abort flag, and the kernel winds down without
+// touching the GPU's health.
 #ifndef FA_WAIT_LIMIT_NS
 #define FA_WAIT_LIMIT_NS 4000000000ull
 #endif
@@ -31,10 +32,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
-
-__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0; }
 
 // ------------------------------------------------------------------ mbarrier
 
@@ -67,10 +64,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Where a CTA records that it gave up, and the device-wide status word.
+// Where a wait that gives up leaves its marks.
+//   status  device-wide report word: the first failure on the device since it was
+//           last read (code << 16 | site).  Only fa_last_device_error() reads it;
+//           no kernel acts on it, so a failure nobody read cannot affect later calls.
+//   call    abort word of the call the kernel belongs to (global memory, zeroed at
+//           the start of that call): the first CTA that gives up sets it, and every
+//           other CTA of the same call then stops waiting at its next slow wait.
+//   abort   shared: set once any warp of this CTA gave up.
 struct WaitCtx {
-  unsigned int* status;   // global: first failure code wins (code << 16 | site)
-  volatile int* abort;    // shared: set once any warp of the CTA gave up
+  unsigned int* status;
+  unsigned int* call;
+  volatile int* abort;
 };
 
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
@@ -80,12 +85,13 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     for (int i = 0; i < 128; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*w.abort) return false;
-    if (*reinterpret_cast<volatile unsigned int*>(w.status) != 0u) {  // another CTA gave up
+    if (*reinterpret_cast<volatile unsigned int*>(w.call) != 0u) {   // another CTA of this call gave up
       *w.abort = 1;
       return false;
     }
     if (globaltimer_ns() - t0 > FA_WAIT_LIMIT_NS) {
       atomicCAS(w.status, 0u, (kStatusTimeout << 16) | site);
+      atomicExch(w.call, 1u);
       *w.abort = 1;
       return false;
     }
@@ -97,11 +103,6 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w, site);
-}
-
-// Named barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------ TMA / bulk
@@ -132,13 +133,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
-}
-
-// Bulk element-wise fp32 add of a shared-memory block into global memory.
-__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-               ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
 }
 
 // Element-wise fp32 add into global memory, performed at L2 (no return value).
@@ -187,32 +181,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc)
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D(tmem) (+)= A(tmem) * B(smem desc)
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(bar) : "memory");
-}
-
 // Warp-wide forms: every lane of a converged warp executes the call with the
 // same (warp-uniform) operands and elect.sync picks the one lane that issues.
 // Keeping the whole warp on the issue path lets descriptors stay warp-uniform.
@@ -250,11 +218,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // 32x32b shape: thread t of a warp whose index w satisfies w % 4 == q accesses
 // TMEM lane 32*q + t; .xN reads/writes N consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-               : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])

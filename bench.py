@@ -452,8 +452,12 @@ def main():
             line["parity"] = dict(par, group="batch 0, kv head 0 with its query heads, full length",
                                   bound="max|gpu - oracle| / (1e-2 max|oracle| + 1e-3), <= 1 passes")
         except Exception as e:   # the measurement line is printed whatever happens here
-            line["cpu_baseline"], _ = run_cpu_baseline(sh)
             line["parity"] = {"error": f"{type(e).__name__}: {e}"}
+            try:
+                line["cpu_baseline"], _ = run_cpu_baseline(sh)
+            except Exception as e2:
+                line["cpu_baseline"] = None
+                line["cpu_baseline_error"] = f"{type(e2).__name__}: {e2}"
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -40,15 +40,25 @@
  * Every pointer is a DEVICE pointer on the current device (except for
  * fa_bwd_host), 16-byte aligned.  The caller owns every buffer (inputs,
  * outputs, workspace, staging) and the stream; the library allocates no
- * device memory, keeps no state besides one status word per kernel family
- * (and fa_bwd_host's copy and slot streams), and never synchronises inside
+ * device memory, keeps no state besides small arrays compiled into it (one
+ * status word per device, 256 forward abort words, fa_bwd_noalloc's scratch)
+ * and fa_bwd_host's copy and slot streams, and never synchronises inside
  * fa_fwd* / fa_bwd*.  All work is enqueued on `stream` (fa_bwd_host forks
  * from it and joins back into it).
  *
  * Errors: each call validates its arguments first and, on failure, returns a
  * non-zero fa_status WITHOUT launching anything.  FA_ERR_CUDA reports a
- * failed launch (cudaGetLastError).  Device-side waits are bounded: a wait
- * that runs out sets a status word read by fa_last_device_error().
+ * failed launch (cudaGetLastError).  Device-side waits are bounded.  A wait
+ * that runs out does two things:
+ *   - it records FA_ERR_DEVICE_TIMEOUT in the device's status word, which
+ *     fa_last_device_error() reads and clears; and
+ *   - it sets the abort word of its own call, so that the other CTAs of that
+ *     call stop waiting and skip their output stores.
+ * Each call has its own abort word: fa_bwd* keeps it in the first 256 bytes
+ * of its workspace (cleared by fa_bwd_preprocess), fa_fwd* takes one of 256
+ * slots in the library and clears it on `stream` before its kernel.  The
+ * status word only reports: no kernel reads it.  A failure left unread
+ * therefore never changes the results of later calls, on any stream.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -106,7 +116,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 
 /*
  * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs.
- * Holds D = rowsum(dO o O) and -L*log2(e) per query row (rows padded to a
+ * Holds the call's abort word (256 bytes), D = rowsum(dO o O) and
+ * -L*log2(e) per query row (rows padded to a
  * multiple of 128), plus, when deterministic == 0, the fp32 dQ accumulator
  * [B, Hq, Nq padded, d] of the sequence-parallel scheme (triton #1806,
  * "Minimal Repro": dq is an fp32 buffer that every KV-tile program adds to).
@@ -185,7 +196,9 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void*
  * Limit: returns FA_ERR_WORKSPACE, launching nothing, when
  * fa_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d, deterministic) exceeds
  * FA_STATIC_SCRATCH_BYTES (deterministic mode needs 8 bytes per query row,
- * rows padded to 128 per head; atomic mode 8 + 4*64 (d <= 64) or 8 + 4*128 bytes per padded row).
+ * rows padded to 128 per head; atomic mode 8 + 4*64 (d <= 64) or 8 + 4*128 bytes
+ * per padded row; plus 256 bytes).  Arguments are checked in fa_bwd's order,
+ * so a call with, say, an unknown dtype gets FA_ERR_DTYPE whatever its size.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture.  All calls share the one array, and each call rewrites
@@ -347,9 +360,10 @@ int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, cons
  * arguments), 256-byte aligned (FA_ERR_ALIGN), not used by anything else until
  * `stream` passes the call (FA_ERR_WORKSPACE if NULL or too small).  Every
  * argument error (shape, dtype, scale, causal, staging) is returned before
- * anything is queued; only FA_ERR_CUDA from a failed copy or launch can leave
- * earlier chunks' work in flight (synchronise the device before reusing the
- * buffers then).
+ * anything is queued.  If a copy or launch fails after work has been queued
+ * (FA_ERR_CUDA), the call first waits for everything it queued on its copy
+ * and slot streams to finish, so no transfer into or out of the caller's
+ * buffers is still running when it returns.
  */
 #define FA_HOST_MAX_SLOTS 8
 
@@ -367,10 +381,14 @@ const char* fa_strerror(int status);
 
 /*
  * fa_last_device_error -- synchronises `stream`, then reads and clears the
- * device status words.  Returns FA_ERR_DEVICE_TIMEOUT if any bounded wait in
- * a kernel ran out since the last call, FA_ERR_ARG if a kernel skipped a
- * packed-batch sequence with out-of-range offsets, FA_ERR_CUDA if the sync
- * failed, FA_OK otherwise.
+ * current device's status word.  Returns FA_ERR_DEVICE_TIMEOUT if any bounded
+ * wait in a kernel ran out since the word was last read, FA_ERR_ARG if a
+ * kernel skipped a packed-batch sequence with out-of-range offsets,
+ * FA_ERR_CUDA if the sync failed, FA_OK otherwise.
+ * The word is one per device, not per stream: it holds the first failure of
+ * any call on the device since the last read, and work on other streams that
+ * has not finished yet may still set it after this returns.  Reading it is
+ * optional; kernels never act on it (see "Errors" above).
  */
 int fa_last_device_error(cudaStream_t stream);
 

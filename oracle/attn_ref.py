@@ -230,12 +230,6 @@ def backward(q, k, v, do, scale: float, causal: bool, lse=None, o=None, groups=N
     return out
 
 
-def backward_flops(B, Hq, Nq, Nkv, d, causal) -> float:
-    """FLOPs counted for the backward: 10 * B * Hq * Nq * Nkv * d, halved when causal."""
-    f = 10.0 * B * Hq * Nq * Nkv * d
-    return f / 2 if causal else f
-
-
 # ------------------------------------------------------------ packed batches
 #
 # Variable-length batches: "[Kernel] Flash attention 2" (Liger-Kernel #275,

@@ -46,16 +46,18 @@ def test_strerror_covers_all_codes(lib):
 
 
 def test_workspace_size_formula(lib):
-    # rows padded to 128: L*log2e and D (fp32 each), plus the fp32 dQ accumulator in atomic mode
+    # 256 bytes for the call's abort word, then rows padded to 128: L*log2e and D (fp32 each),
+    # plus the fp32 dQ accumulator in atomic mode
     rows = 2 * 4 * 128
-    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 1) == 2 * rows * 4
-    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 0) == 2 * rows * 4 + rows * 64 * 4
+    hdr = 256
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 1) == hdr + 2 * rows * 4
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 64, 0) == hdr + 2 * rows * 4 + rows * 64 * 4
     assert _lib.fa_bwd_workspace_size(2, 4, 3, 100, 100, 64, 0) == 0     # GQA mismatch
     assert _lib.fa_bwd_workspace_size(2, 4, 4, 0, 100, 64, 0) == 0       # empty sequence
     assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 100, 0) == 0    # head dim
     # other head dims use the accumulator width of the kernel that serves them (64 or 128)
-    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 96, 0) == 2 * rows * 4 + rows * 128 * 4
-    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 40, 0) == 2 * rows * 4 + rows * 64 * 4
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 96, 0) == hdr + 2 * rows * 4 + rows * 128 * 4
+    assert _lib.fa_bwd_workspace_size(2, 4, 4, 100, 100, 40, 0) == hdr + 2 * rows * 4 + rows * 64 * 4
 
 
 def _bwd(**kw):
@@ -244,3 +246,14 @@ def test_host_pipeline_validation_and_staging_size(lib):
     assert _lib.fa_bwd_host(*base, 0.1, 1, 7, 0, 2, 2, W, 1 << 30) == _lib.FA_ERR_DTYPE
     assert _lib.fa_bwd_host(*base, float("nan"), 1, _lib.FA_BF16, 0, 2, 2, W, 1 << 30) == _lib.FA_ERR_ARG
     assert _lib.fa_bwd_host(*base, 0.1, 3, _lib.FA_BF16, 0, 2, 2, W, 1 << 30) == _lib.FA_ERR_ARG
+
+
+def test_noalloc_checks_dtype_and_arguments_before_its_size_limit(lib):
+    # the headline problem in atomic mode does not fit the static scratch ...
+    assert _lib.fa_bwd_workspace_size(4, 32, 8, 8192, 8192, 128, 0) > _lib.FA_STATIC_SCRATCH_BYTES
+    args = [A] * 9 + [4, 32, 8, 8192, 8192, 128]
+    assert _lib.fa_bwd_noalloc(*args, 0.088, 1, _lib.FA_BF16, 0, None) == _lib.FA_ERR_WORKSPACE
+    # ... but an unknown dtype, a scale that is not finite or an unknown causal mode is named first
+    assert _lib.fa_bwd_noalloc(*args, 0.088, 1, 7, 0, None) == _lib.FA_ERR_DTYPE
+    assert _lib.fa_bwd_noalloc(*args, float("nan"), 1, _lib.FA_BF16, 0, None) == _lib.FA_ERR_ARG
+    assert _lib.fa_bwd_noalloc(*args, 0.088, 3, _lib.FA_BF16, 0, None) == _lib.FA_ERR_ARG
