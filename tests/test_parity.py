@@ -108,7 +108,7 @@ def test_llama_gqa_full(n):
     check_full(inputs.llama_gqa(n), 5, False)
 
 
-@pytest.mark.parametrize("n", [96, 1000])
+@pytest.mark.parametrize("n", [32, 96, 256, 512, 1000])
 def test_llama_gqa_full_deterministic(n):
     check_full(inputs.llama_gqa(n), 5, True)
 
@@ -136,9 +136,19 @@ def test_llama_gqa_sampled(n):
         pairs[f"dV[{b},{g}]"] = (_np(dv[b:b + 1, g:g + 1]), r["dv"])
     fails, rep = errors(pairs)
     assert not fails, rep
-    # a property that holds on every head: sum over keys of dK is exactly zero
-    col = dk.float().sum(dim=2).abs().max().item()
-    assert col <= 1e-2 * dk.float().abs().max().item() * shape.Nkv ** 0.5, col
+    # A property that holds on every head: the sum of dK over the keys is exactly zero (each
+    # row of dS sums to zero).  What remains on the GPU comes from rounding dS and dK to 16
+    # bits.  On the sampled groups that residue must stay within 4x of the residue that
+    # rounding the oracle's own dK to bf16 leaves; on every head within 0.1 of its max |dK|
+    # (measured: at most 0.031 up to N = 16384).
+    def residue(x):                      # max_c |sum_j x_jc| / max |x|, per (batch, kv head)
+        x = torch.as_tensor(x).double()
+        return x.sum(dim=-2).abs().amax(-1) / x.abs().amax((-2, -1))
+    for b, g in groups:
+        floor = residue(torch.from_numpy(pairs[f"dK[{b},{g}]"][1]).to(torch.bfloat16)).max().item()
+        got = residue(dk[b:b + 1, g:g + 1].cpu()).max().item()
+        assert got <= 4 * floor + 1e-3, (b, g, got, floor)
+    assert residue(dk.cpu()).max().item() <= 0.1
 
 
 # ------------------------------------------------------------ extra shapes
