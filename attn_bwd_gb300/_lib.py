@@ -13,7 +13,9 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libattn_bwd_gb300.so")
+# ATTN_BWD_GB300_LIB may name another build of the same library (e.g. the bounds-checking
+# debug build, libattn_bwd_gb300_bounds.so); it is read once, at import.
+LIB_PATH = os.environ.get("ATTN_BWD_GB300_LIB") or os.path.join(_HERE, "libattn_bwd_gb300.so")
 
 FA_OK = 0
 FA_ERR_NULL = 1
@@ -26,6 +28,7 @@ FA_ERR_DTYPE = 7
 FA_ERR_CUDA = 8
 FA_ERR_DEVICE_TIMEOUT = 9
 FA_ERR_ARG = 10
+FA_ERR_BOUNDS = 11
 FA_F16 = 0
 FA_BF16 = 1
 FA_CAUSAL_NONE = 0

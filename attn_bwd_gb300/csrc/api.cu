@@ -430,6 +430,7 @@ const char* fa_strerror(int status) {
     case FA_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case FA_ERR_ARG: return "an argument is out of range";
+    case FA_ERR_BOUNDS: return "a kernel's bounds check failed (debug build)";
     default: return "unknown fa_status";
   }
 }
@@ -571,7 +572,7 @@ int fa_last_device_error(cudaStream_t stream) {
     const unsigned int zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
     const int code = static_cast<int>(v >> 16);
-    return code == FA_ERR_DEVICE_TIMEOUT || code == FA_ERR_ARG ? code : FA_ERR_CUDA;
+    return code == FA_ERR_DEVICE_TIMEOUT || code == FA_ERR_ARG || code == FA_ERR_BOUNDS ? code : FA_ERR_CUDA;
   }
   return FA_OK;
 }

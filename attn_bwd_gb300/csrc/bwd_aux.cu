@@ -59,7 +59,7 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
     const bool live = valid && r < sq.nq;
     const long long qrow = sq.q_start + r;
     float acc = 0.f;
-    if (live && 8 * sub < m.d) {
+    if (live && 8 * sub < m.d && FA_BOUNDS_S(qrow < rows_q(m), status, 90)) {
       float a[8], g[8];
       widen8<BF16>(__ldg(o + at(m.st.o, m, b, h, qrow) / 8 + sub), a);
       widen8<BF16>(__ldg(dO + at(m.st.dO, m, b, h, qrow) / 8 + sub), g);
@@ -100,7 +100,7 @@ dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq, long l
     const int b = static_cast<int>(bh / m.Hq);
     const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
     const Seq sq = seq_of(m, b, status, 31);
-    if (r >= sq.nq || 8 * c8 >= m.d) continue;
+    if (r >= sq.nq || 8 * c8 >= m.d || !FA_BOUNDS_S(sq.q_start + r < rows_q(m), status, 91)) continue;
     const long long src = (row * D) / 4 + 2 * c8;
     const float4 a = __ldcs(acc + src);
     const float4 c = __ldcs(acc + src + 1);
@@ -155,7 +155,7 @@ dbias_zero_kernel(SeqMap m, long long rows, unsigned int* status) {
     const int b = static_cast<int>(bh / m.Hq);
     const int h = static_cast<int>(bh - static_cast<long long>(b) * m.Hq);
     const Seq sq = seq_of(m, b, status, 32);
-    if (q >= sq.nq) continue;
+    if (q >= sq.nq || !FA_BOUNDS_S(q < m.Nq && h < m.Hq && b < m.B, status, 92)) continue;
     const long long first = static_cast<long long>(q / kMainBM + 1) * kMainBM + sq.delta;
     const long long k0 = (first <= 0 ? 0 : (first + kMainBN - 1) / kMainBN) * kMainBN;
     uint16_t* dst = static_cast<uint16_t*>(m.dbias) + bias_row(m.dbias_st, b, h, q);

@@ -156,7 +156,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0) {
+    const size_t ws_rows = static_cast<size_t>(p.B) * p.Hq * p.NqPad;
+    // (a tile past its sequence's end, T == 0, is still loaded -- from the next sequence's
+    // rows or as zero fill -- and never used)
+    if (lane == 0 && FA_BOUNDS(h < p.Hq && bc < batch_extent(p.m) &&
+                                   (q0 >= sq.nq || sq.q_start + q0 < rows_q(p.m)) &&
+                                   static_cast<size_t>(bh) * p.NqPad + q0 + BQ <= ws_rows,
+                               wc, 70)) {
       mbar_arrive_expect_tx(bar(B_Q), 2 * L::TILE + 2 * BQ * 4);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
@@ -171,6 +177,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // K(t) once dQ(t - KST) has read its slot; V(t) once dP(t - VST) has read its slot
         // (dP(t - 2) completes before dQ(t - 2), so the V wait never holds back K(t + 1))
         const int ks = t % KST, vs = t % VST;
+        if (!FA_BOUNDS(sq.k_start + t * BK < rows_k(p.m) && hk < p.Hkv, wc, 71)) break;
         if (t >= KST && !mbar_wait(bar(B_KEMPTY + ks), ((t / KST) & 1) ^ 1, wc, 21)) break;
         mbar_arrive_expect_tx(bar(B_KFULL + ks), L::TILE);
 #pragma unroll
@@ -351,7 +358,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      if (q < sq.nq && !aborted) {
+      if (q < sq.nq && !aborted && FA_BOUNDS(sq.q_start + q < rows_q(p.m), wc, 72)) {
         uint4* d4 = reinterpret_cast<uint4*>(out + col * 2);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)

@@ -236,8 +236,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0 && T > 0) {
-      const int bc = bcoord(p.m, b);                      // batch coordinate in the tensor maps
+    const int bc = bcoord(p.m, b);                        // batch coordinate in the tensor maps
+    if (lane == 0 && T > 0 &&
+        FA_BOUNDS(sq.k_start + kv0 < rows_k(p.m) && hkv < p.Hkv && bc < batch_extent(p.m), wc, 60)) {
       mbar_arrive_expect_tx(bar(BR::KV), 2 * L::KV_BYTES);
 #pragma unroll
       for (int hh = 0; hh < L::NH; ++hh) {
@@ -252,6 +253,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int h = hkv * G + t / per_head;
         const int q0 = (i0 + t % per_head) * BM;
         const int bh = b * p.Hq + h;                      // workspace rows are (b, h, padded q)
+        if (!FA_BOUNDS(h < p.Hq && q0 < sq.nq && sq.q_start + q0 < rows_q(p.m) &&
+                           static_cast<size_t>(bh) * p.NqPad + q0 + BM <= static_cast<size_t>(p.B) * p.Hq * p.NqPad,
+                       wc, 61))
+          break;
+        if constexpr (BIAS)
+          if (!FA_BOUNDS(kv0 < p.Nkv && (p.m.bias_st.n == 0 || q0 < p.Nq) && h < p.Hq && b < p.B, wc, 63)) break;
         const uint32_t fb = bar(BR::QFULL + s);
         mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + L::LD_BYTES);
 #pragma unroll
@@ -527,7 +534,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (lane == 0) mbar_arrive(bar(BR::DBFULL + grp));
             if ((warp & 3) == 0) {                          // the group's first warp issues the store
               if (!__all_sync(0xffffffffu, mbar_wait(bar(BR::DBFULL + grp), n_db & 1, wc, 19))) break;
-              if (lane == 0) {
+              if (lane == 0 && FA_BOUNDS(kv0 < p.Nkv && qc < p.Nq && h < p.Hq && b < p.B, wc, 66)) {
                 tma_store_4d(&tm_dbias, smem_u32(half), kv0, qc, h, b);
                 bulk_commit_group();
               }
@@ -580,7 +587,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0) mbar_arrive(bar(BR::DQEMPTY));
         // Thread r holds column r of the 64 x d tile: for each query row, the 32
         // lanes of a warp add one contiguous 128-byte segment of the accumulator.
-        if (r < D) {
+        if (r < D && FA_BOUNDS(static_cast<size_t>(b * p.Hq + h) * p.NqPad + q0 + BM <=
+                                   static_cast<size_t>(p.B) * p.Hq * p.NqPad,
+                               wc, 64)) {
           float* dst = p.dq_acc + (static_cast<size_t>(b * p.Hq + h) * p.NqPad + q0) * D + r;
 #pragma unroll
           for (int c = 0; c < 32; ++c) red_add_f32(dst + c * D, __uint_as_float(v0[c]));
@@ -625,7 +634,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      if (kv < sq.nk && !aborted) store_row_chunk<BF16>(out + ch * 64, pk, p.m.d - 32 * ch);
+      if (kv < sq.nk && !aborted && FA_BOUNDS(sq.k_start + kv < rows_k(p.m), wc, 65))
+        store_row_chunk<BF16>(out + ch * 64, pk, p.m.d - 32 * ch);
     }
   }
 

@@ -170,7 +170,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0 && T > 0) {
+    if (lane == 0 && T > 0 &&
+        FA_BOUNDS(h < p.Hq && bc < batch_extent(p.m) && sq.q_start + q0 < rows_q(p.m), wc, 80)) {
       mbar_arrive_expect_tx(bar(B_Q), NT * L::TILE);
 #pragma unroll
       for (int x = 0; x < NT; ++x)
@@ -182,6 +183,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int t = 0; t < T; ++t) {
         const int s = t % STAGES;
         const uint32_t ph = (t / STAGES) & 1;
+        if (!FA_BOUNDS(sq.k_start + t * BK < rows_k(p.m) && hk < p.Hkv, wc, 81)) break;
+        if constexpr (BIAS)
+          if (!FA_BOUNDS(t * BK < p.Nkv && (p.m.bias_st.n == 0 || q0 < p.Nq) && h < p.Hq && b < p.B, wc, 82)) break;
         if (t >= STAGES && !mbar_wait(bar(B_KVEMPTY + s), ph ^ 1, wc, 51)) break;
         const uint32_t fb = bar(B_KVFULL + s);
         mbar_arrive_expect_tx(fb, 2 * L::TILE);
@@ -409,7 +413,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       have = __all_sync(0xffffffffu, mbar_wait(bar(B_PV + qt), (T - 1) & 1, wc, 58));
       tc_fence_after();
     }
-    const bool aborted = *abort_flag != 0;
+    const bool aborted = *abort_flag != 0 || !(q < sq.nq ? FA_BOUNDS(sq.q_start + q < rows_q(p.m), wc, 83) : true);
     const float inv = l > 0.f ? 1.f / l : 0.f;         // a row that saw no key: O = 0
     uint8_t* out = reinterpret_cast<uint8_t*>(p.o) + at(p.m.st.o, p.m, b, h, sq.q_start + q) * 2;
 #pragma unroll 1

@@ -98,6 +98,30 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
+// Bounds checks of the debug build (compiled with -DFA_DEBUG_BOUNDS).  Each check
+// guards one memory access: a TMA tile coordinate, a bulk copy's range, or the index
+// of a global store or reduction, against the extents the kernel was given.  A check
+// that fails records FA_ERR_BOUNDS (11) with its site in the status word, raises the
+// call's abort word and the CTA's abort flag (so the CTA winds down as after a
+// timeout), and the guarded access is skipped.  In the normal build the condition is
+// not even evaluated.
+constexpr unsigned kStatusBounds = 11u;
+
+#ifdef FA_DEBUG_BOUNDS
+static __device__ __noinline__ bool bounds_fail(unsigned int* status, unsigned int* call, volatile int* abort,
+                                                uint32_t site) {
+  atomicCAS(status, 0u, (kStatusBounds << 16) | site);
+  if (call) atomicExch(call, 1u);
+  if (abort) *abort = 1;
+  return false;
+}
+#define FA_BOUNDS(cond, wc, site) ((cond) || ::fa::bounds_fail((wc).status, (wc).call, (wc).abort, (site)))
+#define FA_BOUNDS_S(cond, status, site) ((cond) || ::fa::bounds_fail((status), nullptr, nullptr, (site)))
+#else
+#define FA_BOUNDS(cond, wc, site) true
+#define FA_BOUNDS_S(cond, status, site) true
+#endif
+
 // Bounded wait for the phase with the given parity to complete.
 // Returns false if the wait gave up (the caller must wind down).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {

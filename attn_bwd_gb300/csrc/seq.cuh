@@ -62,6 +62,12 @@ __device__ __forceinline__ Seq seq_of(const SeqMap& m, int b, unsigned int* stat
 // has one: its sequences are told apart by their rows).
 __device__ __forceinline__ int bcoord(const SeqMap& m, int b) { return m.cu_q ? 0 : b; }
 
+// Extents of the tensors (those of their tensor maps): rows along each head's row
+// axis of the Q-like and K-like tensors, and the batch extent.
+__device__ __forceinline__ int rows_q(const SeqMap& m) { return m.cu_q ? m.total_q : m.Nq; }
+__device__ __forceinline__ int rows_k(const SeqMap& m) { return m.cu_q ? m.total_k : m.Nkv; }
+__device__ __forceinline__ int batch_extent(const SeqMap& m) { return m.cu_q ? 1 : m.B; }
+
 // Element offset of row `row` of head h of sequence b in a tensor with strides s
 // (row already includes the sequence's first row).
 __device__ __forceinline__ long long at(const Str3& s, const SeqMap& m, int b, int h, long long row) {

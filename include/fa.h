@@ -81,7 +81,8 @@ typedef enum {
   FA_ERR_DTYPE = 7,           /* dtype not an fa_dtype value                        */
   FA_ERR_CUDA = 8,            /* a CUDA launch or driver call failed                */
   FA_ERR_DEVICE_TIMEOUT = 9,  /* a bounded device-side wait ran out (see fa_last_device_error) */
-  FA_ERR_ARG = 10             /* another argument is out of range (scale not finite, causal unknown, ...) */
+  FA_ERR_ARG = 10,            /* another argument is out of range (scale not finite, causal unknown, ...) */
+  FA_ERR_BOUNDS = 11          /* a kernel's bounds check failed (debug builds with FA_DEBUG_BOUNDS only) */
 } fa_status;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -384,6 +385,7 @@ const char* fa_strerror(int status);
  * current device's status word.  Returns FA_ERR_DEVICE_TIMEOUT if any bounded
  * wait in a kernel ran out since the word was last read, FA_ERR_ARG if a
  * kernel skipped a packed-batch sequence with out-of-range offsets,
+ * FA_ERR_BOUNDS if a bounds check of the debug build failed,
  * FA_ERR_CUDA if the sync failed, FA_OK otherwise.
  * The word is one per device, not per stream: it holds the first failure of
  * any call on the device since the last read, and work on other streams that
@@ -391,6 +393,17 @@ const char* fa_strerror(int status);
  * optional; kernels never act on it (see "Errors" above).
  */
 int fa_last_device_error(cudaStream_t stream);
+
+/*
+ * Debug build.  The library compiled with -DFA_DEBUG_BOUNDS (python -m
+ * attn_bwd_gb300.build --debug-bounds: libattn_bwd_gb300_bounds.so) has the
+ * same entry points; its kernels check every TMA tile coordinate, bulk copy
+ * range and global store or reduction index against the extents of the
+ * tensors they were given.  A failed check is recorded like a timeout
+ * (fa_last_device_error() returns FA_ERR_BOUNDS), aborts the call, and the
+ * access is skipped, so nothing outside a tensor is touched.  The normal
+ * build compiles no checks.
+ */
 
 /*
  * fa_selftest_wait_timeout -- launches one CTA that waits on a barrier no one

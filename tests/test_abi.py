@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_strerror_covers_all_codes(lib):
-    for code in range(0, 11):
+    for code in range(0, 12):
         assert _lib.fa_strerror(code) != "unknown fa_status"
     assert _lib.fa_strerror(1234) == "unknown fa_status"
 
