@@ -169,14 +169,7 @@ dbias_zero_kernel(SeqMap m, long long rows, unsigned int* status) {
   }
 }
 
-// SM count of the current device (the grid-stride kernels launch up to 16 blocks per SM).
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-    return 1;
-  return n;
-}
-
+// Grid of a grid-stride kernel: enough blocks for the work, at most 16 per SM.
 long long grid_for(long long work_items, int per_block) {
   long long g = (work_items + per_block - 1) / per_block;
   const long long cap = static_cast<long long>(sm_count()) * 16;

@@ -687,6 +687,7 @@ cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUte
                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
                             const CUtensorMap& tdb, cudaStream_t stream) {
   const bool det = a.pb.deterministic != 0;
+  if (use_persistent(a.pb)) return launch_bwd_main_persist(a, tq, tdo, tk, tv, stream);
   if (a.pb.d > 64) {
     if (a.pb.bf16) return det ? launch_b<128, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
                               : launch_b<128, true, false>(a, tq, tdo, tk, tv, tb, tdb, stream);

@@ -19,6 +19,15 @@ constexpr int kMainBM = 64;
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
+// SM count of the current device (1 if it cannot be read).
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
 // Workspace carve-up shared by every stage of the backward.
 struct Workspace {
   unsigned int* abort;   // the call's abort word (first 256 bytes): zeroed by the preprocess
@@ -130,6 +139,13 @@ cudaError_t launch_dbias_zero(const Problem& pb, unsigned int* status, cudaStrea
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
                             const CUtensorMap& tdb, cudaStream_t stream);
+
+// bwd_main_persist.cu: the same products as a persistent kernel (one CTA per SM walking
+// the work items back to back), which launch_bwd_main uses for every problem without an
+// additive bias; maps as for bwd_main.cu
+inline bool use_persistent(const Problem& pb) { return pb.bias == nullptr; }
+cudaError_t launch_bwd_main_persist(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
+                                    const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
 // bwd_dq.cu: maps are Q, dO (box 64 x 128 rows), K, V (box 64 x 128 rows)
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,

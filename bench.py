@@ -105,7 +105,7 @@ def load_peaks():
 
 def main_kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("bwd_main.cu", "ptx.cuh"):
+    for f in ("bwd_main_persist.cu", "bwd_main.cu", "ptx.cuh", "kernels.h"):
         with open(os.path.join(ROOT, "attn_bwd_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
