@@ -1,4 +1,7 @@
-// bwd_main.cu -- KV-tile-parallel attention backward on tcgen05 tensor cores.
+// bwd_main.cu -- KV-tile-parallel attention backward on tcgen05 tensor cores,
+// one CTA per work item.  Problems without an additive bias run the same
+// products in the persistent schedule of bwd_main_persist.cu; this kernel is
+// launched for the bias path (it stages bias tiles and stores dBias).
 //
 // Decomposition: the sequence-parallel scheme of "Extra transposes cause 8x
 // speedup for sequence-parallel Flash Attention backward" (triton #1806,
@@ -109,7 +112,7 @@ struct Bars {
                        DSFREE = DP + 5, ACC = DP + 6, AFIN = DP + 7, BFULL = DP + 8, BEMPTY = BFULL + BSTAGES,
                        DBFULL = BEMPTY + BSTAGES, DBFREE = DBFULL + 2, END = DBFREE + 2;
 };
-static_assert(Bars<4>::END <= Layout<128, false>::NBAR && Bars<3>::END <= Layout<128, true>::NBAR, "barrier count");
+static_assert(Bars<3>::END <= Layout<128, true>::NBAR, "barrier count");
 
 struct Params {
   const float* nLg;
@@ -674,30 +677,25 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool DET>
-cudaError_t launch_b(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                     const CUtensorMap& tv, const CUtensorMap& tb, const CUtensorMap& tdb, cudaStream_t stream) {
-  return a.pb.bias != nullptr ? launch_t<D, BF16, DET, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
-                              : launch_t<D, BF16, DET, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
-}
-
 }  // namespace
 
+// Problems without a bias run the persistent form of this kernel (bwd_main_persist.cu);
+// this one serves the bias path, so only its BIAS = true instantiations are launched.
 cudaError_t launch_bwd_main(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
                             const CUtensorMap& tdb, cudaStream_t stream) {
-  const bool det = a.pb.deterministic != 0;
   if (use_persistent(a.pb)) return launch_bwd_main_persist(a, tq, tdo, tk, tv, stream);
+  const bool det = a.pb.deterministic != 0;
   if (a.pb.d > 64) {
-    if (a.pb.bf16) return det ? launch_b<128, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
-                              : launch_b<128, true, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
-    return det ? launch_b<128, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
-               : launch_b<128, false, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
+    if (a.pb.bf16) return det ? launch_t<128, true, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+                              : launch_t<128, true, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream);
+    return det ? launch_t<128, false, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+               : launch_t<128, false, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream);
   }
-  if (a.pb.bf16) return det ? launch_b<64, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
-                            : launch_b<64, true, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
-  return det ? launch_b<64, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
-             : launch_b<64, false, false>(a, tq, tdo, tk, tv, tb, tdb, stream);
+  if (a.pb.bf16) return det ? launch_t<64, true, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+                            : launch_t<64, true, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream);
+  return det ? launch_t<64, false, true, true>(a, tq, tdo, tk, tv, tb, tdb, stream)
+             : launch_t<64, false, false, true>(a, tq, tdo, tk, tv, tb, tdb, stream);
 }
 
 }  // namespace fa

@@ -14,7 +14,8 @@
 //     the producer loads the next item's first Q/dO tiles while the current
 //     item is computed;
 //   - K and V of the next item are loaded (by a warp of their own) as soon as
-//     the current item's last products have read them;
+//     the current item's last products have read them, or, for d <= 64, where
+//     two K/V buffers fit next to the ring, while the current item is computed;
 //   - the softmax warps write an item's dK/dV while the MMA warps already
 //     compute S^T and dP^T of the next item; the next item's first dV/dK
 //     product waits only for that read-out.
@@ -46,9 +47,11 @@ struct PLayout {
   static constexpr int QHALF = BM * 128;          // bytes of one half of a Q/dO tile
   static constexpr int KV_BYTES = NH * KHALF;     // one K (or V) tile
   static constexpr int Q_BYTES = NH * QHALF;
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = KV_BYTES;
-  static constexpr int OFF_Q = 2 * KV_BYTES;
+  // K/V buffers: two where they fit next to a 4-stage Q/dO ring (d <= 64), so that the
+  // next item's K and V load while the current item is computed; else one
+  static constexpr int KVBUF = D <= 64 ? 2 : 1;
+  static constexpr int OFF_KV = 0;                // buffer k: K at OFF_KV + 2k KV_BYTES, V after it
+  static constexpr int OFF_Q = 2 * KVBUF * KV_BYTES;
   static constexpr int OFF_DO = OFF_Q + QST * Q_BYTES;
   static constexpr int OFF_DS = OFF_DO + QST * Q_BYTES;
   static constexpr int DS_BYTES = BN * BM * 2;    // dS^T, 128 rows x 128 B
@@ -69,9 +72,10 @@ struct PLayout {
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-// barrier indices; S, P, SFREE have one barrier per S^T buffer (tile g uses g & 1)
+// barrier indices; S, P, SFREE have one barrier per S^T buffer (tile g uses g & 1),
+// KVFULL, KVEMPTY one per K/V buffer (item n uses n % KVBUF)
 enum : int {
-  KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + QST, S = QEMPTY + QST, P = S + 2, SFREE = P + 2,
+  KVFULL = 0, KVEMPTY = 2, QFULL = 4, QEMPTY = QFULL + QST, S = QEMPTY + QST, P = S + 2, SFREE = P + 2,
   DP = SFREE + 2, DPFREE, DS, DQFULL, DQEMPTY, DSFREE, ACC, ACCFREE, AFIN1, AFIN2, BAR_END
 };
 static_assert(BAR_END <= PLayout<128>::NBAR, "barrier count");
@@ -162,8 +166,10 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   // every role walks the same items: it = item_of(k, ...) for k = 0, 1, ... while it >= 0
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(KVFULL), 1);
-    mbar_init(bar(KVEMPTY), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(KVFULL + k), 1);
+      mbar_init(bar(KVEMPTY + k), 1);
+    }
     for (int s = 0; s < QST; ++s) {
       mbar_init(bar(QFULL + s), 1);
       mbar_init(bar(QEMPTY + s), 1);
@@ -234,25 +240,30 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     }
   } else if (warp == 3) {
     // ================================================================ TMA producer: K, V
-    // Item n's K and V go into the one K/V buffer once item n - 1's last products have
-    // read it (its Q/dO tiles are already being prefetched by warp 0).
+    // Item n's K and V go into buffer n % KVBUF once the item that used it before
+    // (n - KVBUF) has had its last products read it; its Q/dO tiles are meanwhile
+    // prefetched by warp 0.
     if (lane == 0) {
+      constexpr int NB = L::KVBUF;
       int n = 0;                 // items with work so far
       for (int k = 0, it; (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
         const int bc = bcoord(p.m, w.b);
-        if (n >= 1 && !mbar_wait(bar(KVEMPTY), (n - 1) & 1, wc, 1)) break;
+        const int kb = n % NB;
+        if (n >= NB && !mbar_wait(bar(KVEMPTY + kb), ((n / NB) - 1) & 1, wc, 1)) break;
         if (!FA_BOUNDS(w.sq.k_start + w.kv0 < rows_k(p.m) && w.hkv < p.Hkv && bc < batch_extent(p.m), wc, 67)) break;
-        mbar_arrive_expect_tx(bar(KVFULL), 2 * L::KV_BYTES);
+        const uint32_t fb = bar(KVFULL + kb);
+        const uint32_t kdst = sb + L::OFF_KV + 2 * kb * L::KV_BYTES;
+        mbar_arrive_expect_tx(fb, 2 * L::KV_BYTES);
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_4d(sb + L::OFF_K + hh * L::KHALF, &tm_k, bar(KVFULL), 64 * hh, w.sq.k_start + w.kv0, w.hkv, bc);
-          tma_load_4d(sb + L::OFF_V + hh * L::KHALF, &tm_v, bar(KVFULL), 64 * hh, w.sq.k_start + w.kv0, w.hkv, bc);
+          tma_load_4d(kdst + hh * L::KHALF, &tm_k, fb, 64 * hh, w.sq.k_start + w.kv0, w.hkv, bc);
+          tma_load_4d(kdst + L::KV_BYTES + hh * L::KHALF, &tm_v, fb, 64 * hh, w.sq.k_start + w.kv0, w.hkv, bc);
         }
         ++n;
       }
-      if (n >= 1) drain_wait(bar(KVFULL), (n - 1) & 1);
+      for (int m = max(0, n - NB); m < n; ++m) drain_wait(bar(KVFULL + m % NB), (m / NB) & 1);
     }
   } else if (warp == 1 || warp == 2) {
     // ================================================================ MMA issuers
@@ -277,11 +288,13 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     int n = 0, g = 0;
     bool ok = true;
     if (warp == 1) {
-      const uint64_t dK_k = sw128_desc(sb + L::OFF_K, 16, 1024), dV_k = sw128_desc(sb + L::OFF_V, 16, 1024);
       for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
-        if (!wait(bar(KVFULL), n & 1, 2)) break;
+        const int kb = n % L::KVBUF;
+        const uint32_t aK = sb + L::OFF_KV + 2 * kb * L::KV_BYTES;
+        const uint64_t dK_k = sw128_desc(aK, 16, 1024), dV_k = sw128_desc(aK + L::KV_BYTES, 16, 1024);
+        if (!wait(bar(KVFULL + kb), (n / L::KVBUF) & 1, 2)) break;
         ++n;
         for (int t = 0; t < w.T; ++t, ++g) {
           // G1: S^T(g) = K Q^T into buffer g & 1, once G3(g - 2) has read the P^T there
@@ -311,10 +324,11 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       umma_commit_warp(bar(AFIN1));
       drain_wait(bar(AFIN1), 0);
     } else {
-      const uint64_t dK_mn = sw128_desc(sb + L::OFF_K, L::KHALF, 1024);
       for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
+        const int kb = n % L::KVBUF;
+        const uint64_t dK_mn = sw128_desc(sb + L::OFF_KV + 2 * kb * L::KV_BYTES, L::KHALF, 1024);
         for (int t = 0; t < w.T; ++t, ++g) {
           // the item's first products start new dK/dV sums: the previous item's must have been read out
           if (t == 0 && n >= 1 && !wait(bar(ACCFREE), (n - 1) & 1, 16)) { ok = false; break; }
@@ -353,7 +367,7 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (!ok) break;
         // every product of the item has been issued: K and V may be replaced once they
         // complete, and dK/dV are final
-        umma_commit_warp(bar(KVEMPTY));
+        umma_commit_warp(bar(KVEMPTY + kb));
         umma_commit_warp(bar(ACC));
         ++n;
       }
