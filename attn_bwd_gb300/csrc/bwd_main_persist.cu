@@ -8,7 +8,9 @@
 // per-tile arithmetic of flash_attention_backward.cu).  What differs is the
 // schedule: one CTA per SM takes work items c, c + grid, c + 2 grid, ... in the
 // launch order of bwd_main.cu (chunks of (batch, kv-head) groups, tile-major,
-// the longest first), and the items flow through it back to back:
+// the longest first), fetching the next item number from a counter in the
+// workspace as the hardware scheduler would start the next CTA, and the items
+// flow through it back to back:
 //   - the Q/dO ring, the two S^T buffers and every per-tile hand-off keep
 //     running across items (their phases follow a tile counter of the CTA), so
 //     the producer loads the next item's first Q/dO tiles while the current
@@ -21,9 +23,9 @@
 //     product waits only for that read-out.
 // With short items (a 256-token head walks 4 query tiles per KV tile) the
 // set-up, load latency and epilogue of every item weigh on its time as much as
-// its tiles; on long ones the schedule costs nothing.  Items are dealt to the CTAs in snake order (CTA c takes items c and
-// 2 grid - 1 - c of the first two rounds, ...), which keeps the longest-first
-// order balanced.  No additive bias (bwd_main.cu serves it).
+// its tiles.  The item numbers reach the CTA's roles through a ring of eight
+// slots in shared memory, filled by the Q/dO producer as it starts each item.
+// No additive bias (bwd_main.cu serves it).
 #include <cstdint>
 #include <climits>
 
@@ -58,9 +60,10 @@ struct PLayout {
   static constexpr int OFF_LD = OFF_DS + DS_BYTES;
   static constexpr int LD_BYTES = 2 * BM * 4;     // -L*log2e and D of one tile
   static constexpr int OFF_BAR = OFF_LD + QST * LD_BYTES;
-  static constexpr int NBAR = 32;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int TOTAL = OFF_MISC + 16;
+  static constexpr int NBAR = 48;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort flag, then the item ring
+  static constexpr int OFF_RING = OFF_MISC + 16;
+  static constexpr int TOTAL = OFF_RING + 8 * 4;
   static constexpr int ALLOC = TOTAL + 1024;      // slack for 1024-byte alignment
   // TMEM columns, as in bwd_main.cu
   static constexpr int COL_DK = 0;
@@ -76,7 +79,8 @@ struct PLayout {
 // KVFULL, KVEMPTY one per K/V buffer (item n uses n % KVBUF)
 enum : int {
   KVFULL = 0, KVEMPTY = 2, QFULL = 4, QEMPTY = QFULL + QST, S = QEMPTY + QST, P = S + 2, SFREE = P + 2,
-  DP = SFREE + 2, DPFREE, DS, DQFULL, DQEMPTY, DSFREE, ACC, ACCFREE, AFIN1, AFIN2, BAR_END
+  DP = SFREE + 2, DPFREE, DS, DQFULL, DQEMPTY, DSFREE, ACC, ACCFREE, AFIN1, AFIN2,
+  ITEM_FULL, ITEM_EMPTY = ITEM_FULL + 8, BAR_END = ITEM_EMPTY + 8
 };
 static_assert(BAR_END <= PLayout<128>::NBAR, "barrier count");
 
@@ -93,13 +97,9 @@ struct Params {
   float scale, scale_log2;
   int causal;
   int items;                  // (batch, kv-head, KV tile) work items
+  unsigned int* next_item;    // workspace: items handed out so far (zero between launches)
+  unsigned int* done_ctas;    // workspace: CTAs that have finished (the last one resets both)
 };
-
-// The k-th work item of CTA c out of `grid` (snake order), or -1 past the end.
-__device__ __forceinline__ int item_of(int k, int c, int grid, int items) {
-  const int it = (k & 1) ? (k + 1) * grid - 1 - c : k * grid + c;
-  return it < items ? it : -1;
-}
 
 // One work item: KV tile j of key/value head hkv of sequence b, and the query
 // tiles [i0, nQt) of each of the G query heads of its group (T tiles in all,
@@ -162,8 +162,7 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   const int G = p.Hq / p.Hkv;
-  const int cta = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
-  // every role walks the same items: it = item_of(k, ...) for k = 0, 1, ... while it >= 0
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::OFF_RING);
 
   if (threadIdx.x == 0) {
     for (int k = 0; k < 2; ++k) {
@@ -189,6 +188,10 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     mbar_init(bar(ACCFREE), 8);        // the item's dK/dV read out of TMEM: one arrival per epilogue warp
     mbar_init(bar(AFIN1), 1);          // warp 1's products have completed (at exit)
     mbar_init(bar(AFIN2), 1);          // warp 2's
+    for (int i = 0; i < 8; ++i) {      // item ring: slot written / read by every other role's warp
+      mbar_init(bar(ITEM_FULL + i), 1);
+      mbar_init(bar(ITEM_EMPTY + i), DET ? 11 : 15);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -201,13 +204,55 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{p.status, p.call_abort, abort_flag};
+  // The k-th item of this CTA, as every role but the fetcher sees it: -1 past the last
+  // item, -2 if the wait gave up.  A whole warp calls take_item, a single lane take_item1;
+  // either releases the slot (one arrival per warp).
+  auto take_item = [&](int k) -> int {
+    const int slot = k & 7;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar(ITEM_FULL + slot), (k >> 3) & 1, wc, 40))) return -2;
+    const int it = ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + slot));
+    return it;
+  };
+  auto take_item1 = [&](int k) -> int {
+    const int slot = k & 7;
+    if (!mbar_wait(bar(ITEM_FULL + slot), (k >> 3) & 1, wc, 41)) return -2;
+    const int it = ring[slot];
+    mbar_arrive(bar(ITEM_EMPTY + slot));
+    return it;
+  };
 
   if (warp == 0) {
     // ================================================================ TMA producer: Q, dO, L, D
     if (lane == 0) {
       int g = 0;                 // tiles issued so far (ring stage g % QST)
       bool ok = true;
-      for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
+      // The fetcher: item numbers from the workspace counter, each taken only when this
+      // producer starts the item (a number taken early would pin a long item to a CTA that
+      // is still busy, as the hardware scheduler never does), into the ring.
+      int fetched = 0;
+      bool ended = false;
+      auto fetch_until = [&](int k) -> bool {
+        while (!ended && fetched <= k) {
+          const int slot = fetched & 7;
+          if (fetched >= 8 && !mbar_wait(bar(ITEM_EMPTY + slot), ((fetched >> 3) - 1) & 1, wc, 42)) return false;
+          int v = static_cast<int>(atomicAdd(p.next_item, 1u));
+          if (v >= p.items) {
+            v = -1;
+            ended = true;
+          }
+          ring[slot] = v;
+          mbar_arrive(bar(ITEM_FULL + slot));
+          ++fetched;
+        }
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        if (!fetch_until(k)) break;
+        if (k >= fetched) break;                  // past the end marker
+        const int it = ring[k & 7];              // written by this thread
+        if (it < 0) break;
         const Item w = decode(it, p, G);
         const int bc = bcoord(p.m, w.b);
         for (int t = 0; t < w.T; ++t, ++g) {
@@ -246,7 +291,9 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     if (lane == 0) {
       constexpr int NB = L::KVBUF;
       int n = 0;                 // items with work so far
-      for (int k = 0, it; (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
+      for (int k = 0;; ++k) {
+        const int it = take_item1(k);
+        if (it < 0) break;
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
         const int bc = bcoord(p.m, w.b);
@@ -288,7 +335,9 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     int n = 0, g = 0;
     bool ok = true;
     if (warp == 1) {
-      for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
+      for (int k = 0; ok; ++k) {
+        const int it = take_item(k);
+        if (it < 0) break;
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
         const int kb = n % L::KVBUF;
@@ -324,7 +373,9 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       umma_commit_warp(bar(AFIN1));
       drain_wait(bar(AFIN1), 0);
     } else {
-      for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
+      for (int k = 0; ok; ++k) {
+        const int it = take_item(k);
+        if (it < 0) break;
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
         const int kb = n % L::KVBUF;
@@ -388,7 +439,9 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const float mul = is_dk ? p.scale : 1.0f;
     int n = 0, g = 0;
     bool ok = true;
-    for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
+    for (int k = 0; ok; ++k) {
+      const int it = take_item(k);
+      if (it < 0) break;
       const Item w = decode(it, p, G);
       const int kv = w.kv0 + r;
       const bool row_ok = kv < w.sq.nk;
@@ -513,7 +566,9 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const uint32_t tdQ = tmem + lane_off + L::COL_DQ;
       int g = 0;
       bool ok = true;
-      for (int k = 0, it; ok && (it = item_of(k, cta, grid, p.items)) >= 0; ++k) {
+      for (int k = 0; ok; ++k) {
+        const int it = take_item(k);
+        if (it < 0) break;
         const Item w = decode(it, p, G);
         if (w.T == 0) continue;
         int h = w.hkv * G, qi = w.i0;
@@ -552,6 +607,12 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // every CTA has stopped fetching when it gets here: the last one resets the counters
+  // for the next launch on this workspace
+  if (threadIdx.x == 0 && atomicAdd(p.done_ctas, 1u) == gridDim.x - 1) {
+    atomicExch(p.next_item, 0u);
+    atomicExch(p.done_ctas, 0u);
+  }
 }
 
 template <int D, bool BF16, bool DET>
@@ -576,6 +637,8 @@ cudaError_t launch_t(const MainArgs& a, const CUtensorMap& tq, const CUtensorMap
   p.m = seq_map(a.pb);
   const long long items = static_cast<long long>((a.pb.Nkv + BN - 1) / BN) * a.pb.B * a.pb.Hkv;
   p.items = static_cast<int>(items);
+  p.next_item = a.ws.abort + 1;
+  p.done_ctas = a.ws.abort + 2;
   const long long grid = items < sm_count() ? items : sm_count();
   kern<<<static_cast<unsigned>(grid), kThreads, L::ALLOC, stream>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();

@@ -31,7 +31,8 @@ inline int sm_count() {
 // Workspace carve-up shared by every stage of the backward.
 struct Workspace {
   unsigned int* abort;   // the call's abort word (first 256 bytes): zeroed by the preprocess
-                         // kernel, set by the first CTA of the main or dQ kernel that gives up
+                         // kernel, set by the first CTA of the main or dQ kernel that gives up;
+                         // words 1 and 2 are the persistent main kernel's item counters
   float* nLg;     // [B*Hq*NqPad]   -L * log2(e); -inf on padding rows
   float* Dv;      // [B*Hq*NqPad]   rowsum(dO o O); 0 on padding rows
   float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
