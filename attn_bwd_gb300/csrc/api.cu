@@ -21,15 +21,18 @@ namespace {
 __device__ unsigned int g_status;
 
 // Abort words of forward calls (a backward call keeps its own in its workspace).
-// Each fa_fwd* call takes the next slot and zeroes it on its stream before the
-// launch, so calls in flight at the same time (up to kFwdSlots) never share one.
+// Call n of a device takes slot n mod kFwdSlots with tag n / kFwdSlots + 1: a tag
+// that no earlier call on that slot had (for 2^32 - 1 rounds of the ring), so the
+// word needs no zeroing before the launch and what an earlier call left in it is
+// never read as this call's abort.  Calls in flight at the same time (up to
+// kFwdSlots) never share a slot.
 constexpr int kFwdSlots = 256;
 __device__ unsigned int g_fwd_abort[kFwdSlots];
 
 constexpr int kMaxDevices = 64;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 unsigned int* g_fwd_abort_ptr[kMaxDevices] = {};
-unsigned int g_fwd_next[kMaxDevices] = {};
+unsigned long long g_fwd_next[kMaxDevices] = {};
 std::mutex g_mu;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -50,8 +53,8 @@ int status_ptr(unsigned int** out) {
   return FA_OK;
 }
 
-// Next forward abort slot of the current device.
-int fwd_abort_slot(unsigned int** out) {
+// Next forward abort slot of the current device and the call's tag for it.
+int fwd_abort_slot(unsigned int** out, unsigned int* tag) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -60,7 +63,9 @@ int fwd_abort_slot(unsigned int** out) {
     if (cudaGetSymbolAddress(&p, g_fwd_abort) != cudaSuccess) return FA_ERR_CUDA;
     g_fwd_abort_ptr[dev] = static_cast<unsigned int*>(p);
   }
-  *out = g_fwd_abort_ptr[dev] + (g_fwd_next[dev]++ % kFwdSlots);
+  const unsigned long long n = g_fwd_next[dev]++;
+  *out = g_fwd_abort_ptr[dev] + n % kFwdSlots;
+  *tag = static_cast<unsigned int>((n / kFwdSlots) % 0xFFFFFFFFull) + 1u;
   return FA_OK;
 }
 
@@ -300,7 +305,8 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   unsigned int* status = nullptr;
   if ((st = status_ptr(&status))) return st;
   unsigned int* call_abort = nullptr;
-  if ((st = fwd_abort_slot(&call_abort))) return st;
+  unsigned int call_tag = 0;
+  if ((st = fwd_abort_slot(&call_abort, &call_tag))) return st;
   CUtensorMap tq, tk, tv;
   const int bf = a.pb.bf16;
   if ((st = map_q(&tq, q, g.st.q, bf, g, 128))) return st;
@@ -309,8 +315,7 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   CUtensorMap tb{};
   if (g.bias != nullptr && (st = make_bias_map(&tb, g.bias, bf, g.Nkv, g.Nq, g.Hq, g.B, g.bias_st, 64, 128)))
     return st;
-  if ((st = cuda_status(cudaMemsetAsync(call_abort, 0, sizeof(unsigned int), stream)))) return st;
-  return cuda_status(launch_fwd(a, tq, tk, tv, tb, status, call_abort, stream));
+  return cuda_status(launch_fwd(a, tq, tk, tv, tb, status, call_abort, call_tag, stream));
 }
 
 int run_preprocess(const Geo& g, const void* o, const void* dO, const float* lse, int dtype, int deterministic,

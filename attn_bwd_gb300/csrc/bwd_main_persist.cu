@@ -203,7 +203,7 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{p.status, p.call_abort, abort_flag};
+  const WaitCtx wc{p.status, p.call_abort, abort_flag, 1u};   // the word is zeroed by the preprocess kernel
   // The k-th item of this CTA, as every role but the fetcher sees it: -1 past the last
   // item, -2 if the wait gave up.  A whole warp calls take_item, a single lane take_item1;
   // either releases the slot (one arrival per warp).

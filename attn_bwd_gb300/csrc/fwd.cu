@@ -79,7 +79,8 @@ struct Params {
   void* o;
   float* lse;
   unsigned int* status;       // device-wide report word
-  unsigned int* call_abort;   // this call's abort word
+  unsigned int* call_abort;   // this call's abort word (a slot of a ring)
+  unsigned int call_tag;      // what this call stores there when it gives up
   SeqMap m;
   int B, Hq, Hkv, Nq, Nkv;   // Nq, Nkv: the longest lengths of a packed batch
   float scale_log2;
@@ -166,7 +167,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{p.status, p.call_abort, abort_flag};
+  const WaitCtx wc{p.status, p.call_abort, abort_flag, p.call_tag};
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -451,7 +452,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 template <int D, bool BF16, bool BIAS>
 cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort, cudaStream_t stream) {
+                     const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort, unsigned int call_tag,
+                     cudaStream_t stream) {
   using L = Layout<D, BIAS>;
   constexpr int NT = L::NT;
   auto kern = fwd_kernel<D, BF16, BIAS>;
@@ -462,6 +464,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.lse = a.lse;
   p.status = status;
   p.call_abort = call_abort;
+  p.call_tag = call_tag;
   p.B = a.pb.B; p.Hq = a.pb.Hq; p.Hkv = a.pb.Hkv; p.Nq = a.pb.Nq; p.Nkv = a.pb.Nkv;
   p.scale_log2 = a.pb.scale * 1.4426950408889634f;
   p.causal = a.pb.causal;
@@ -475,20 +478,20 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort,
-                       cudaStream_t stream) {
+                       unsigned int call_tag, cudaStream_t stream) {
   const bool bias = a.pb.bias != nullptr;
   if (a.pb.d > 64) {
     if (a.pb.bf16)
-      return bias ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, call_abort, stream)
-                  : launch_t<128, true, false>(a, tq, tk, tv, tb, status, call_abort, stream);
-    return bias ? launch_t<128, false, true>(a, tq, tk, tv, tb, status, call_abort, stream)
-                : launch_t<128, false, false>(a, tq, tk, tv, tb, status, call_abort, stream);
+      return bias ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
+                  : launch_t<128, true, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
+    return bias ? launch_t<128, false, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
+                : launch_t<128, false, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
   }
   if (a.pb.bf16)
-    return bias ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, call_abort, stream)
-                : launch_t<64, true, false>(a, tq, tk, tv, tb, status, call_abort, stream);
-  return bias ? launch_t<64, false, true>(a, tq, tk, tv, tb, status, call_abort, stream)
-              : launch_t<64, false, false>(a, tq, tk, tv, tb, status, call_abort, stream);
+    return bias ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
+                : launch_t<64, true, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
+  return bias ? launch_t<64, false, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
+              : launch_t<64, false, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
 }
 
 }  // namespace fa

@@ -154,9 +154,10 @@ cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUte
 
 // fwd.cu: maps are Q, K, V (box 64 x 128 rows) and the bias (box 64 keys x 128 queries,
 // 128-byte swizzle; used only when the problem has a bias)
-// `call_abort` is the call's abort word, zeroed on the stream before the launch.
+// `call_abort` is the call's abort word (a slot of a ring) and `call_tag` the value the
+// call stores there when it gives up; no earlier user of the slot had that tag.
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort,
-                       cudaStream_t stream);
+                       unsigned int call_tag, cudaStream_t stream);
 
 }  // namespace fa

@@ -68,14 +68,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 //   status  device-wide report word: the first failure on the device since it was
 //           last read (code << 16 | site).  Only fa_last_device_error() reads it;
 //           no kernel acts on it, so a failure nobody read cannot affect later calls.
-//   call    abort word of the call the kernel belongs to (global memory, zeroed at
-//           the start of that call): the first CTA that gives up sets it, and every
-//           other CTA of the same call then stops waiting at its next slow wait.
+//   call    abort word of the call the kernel belongs to (global memory): the first
+//           CTA that gives up stores the call's tag in it, and every other CTA of the
+//           same call then stops waiting at its next slow wait.
 //   abort   shared: set once any warp of this CTA gave up.
+//   tag     the value that means "this call gave up".  A backward call's word is in
+//           its workspace and zeroed at the start of the call (tag 1); a forward call
+//           takes a slot in a ring of words and a tag no earlier user of that slot
+//           had, so the word needs no zeroing and a stale value never matches.
 struct WaitCtx {
   unsigned int* status;
   unsigned int* call;
   volatile int* abort;
+  unsigned int tag;
 };
 
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
@@ -85,13 +90,13 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     for (int i = 0; i < 128; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*w.abort) return false;
-    if (*reinterpret_cast<volatile unsigned int*>(w.call) != 0u) {   // another CTA of this call gave up
+    if (*reinterpret_cast<volatile unsigned int*>(w.call) == w.tag) {   // another CTA of this call gave up
       *w.abort = 1;
       return false;
     }
     if (globaltimer_ns() - t0 > FA_WAIT_LIMIT_NS) {
       atomicCAS(w.status, 0u, (kStatusTimeout << 16) | site);
-      atomicExch(w.call, 1u);
+      atomicExch(w.call, w.tag);
       *w.abort = 1;
       return false;
     }
@@ -108,15 +113,16 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 constexpr unsigned kStatusBounds = 11u;
 
 #ifdef FA_DEBUG_BOUNDS
-static __device__ __noinline__ bool bounds_fail(unsigned int* status, unsigned int* call, volatile int* abort,
-                                                uint32_t site) {
+static __device__ __noinline__ bool bounds_fail(unsigned int* status, unsigned int* call, unsigned int tag,
+                                                volatile int* abort, uint32_t site) {
   atomicCAS(status, 0u, (kStatusBounds << 16) | site);
-  if (call) atomicExch(call, 1u);
+  if (call) atomicExch(call, tag);
   if (abort) *abort = 1;
   return false;
 }
-#define FA_BOUNDS(cond, wc, site) ((cond) || ::fa::bounds_fail((wc).status, (wc).call, (wc).abort, (site)))
-#define FA_BOUNDS_S(cond, status, site) ((cond) || ::fa::bounds_fail((status), nullptr, nullptr, (site)))
+#define FA_BOUNDS(cond, wc, site) \
+  ((cond) || ::fa::bounds_fail((wc).status, (wc).call, (wc).tag, (wc).abort, (site)))
+#define FA_BOUNDS_S(cond, status, site) ((cond) || ::fa::bounds_fail((status), nullptr, 0u, nullptr, (site)))
 #else
 #define FA_BOUNDS(cond, wc, site) true
 #define FA_BOUNDS_S(cond, status, site) true

@@ -55,9 +55,11 @@
  *   - it sets the abort word of its own call, so that the other CTAs of that
  *     call stop waiting and skip their output stores.
  * Each call has its own abort word: fa_bwd* keeps it in the first 256 bytes
- * of its workspace (cleared by fa_bwd_preprocess), fa_fwd* takes one of 256
- * slots in the library and clears it on `stream` before its kernel.  The
- * status word only reports: no kernel reads it.  A failure left unread
+ * of its workspace (cleared by fa_bwd_preprocess); fa_fwd* takes the next of
+ * 256 slots in the library together with a value that no earlier call on
+ * that slot used, and a slot aborts a forward only when it holds that call's
+ * value, so nothing is cleared before the kernel.  The status word only
+ * reports: no kernel reads it.  A failure left unread
  * therefore never changes the results of later calls, on any stream.
  */
 #ifndef FA_H_

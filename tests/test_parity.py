@@ -190,6 +190,42 @@ def test_preprocess_rowdot_and_padding():
     assert (acc == 0).all()
 
 
+@pytest.mark.parametrize("det", [False, True], ids=["atomic", "deterministic"])
+@pytest.mark.parametrize("shape", [
+    inputs.Shape(2, 4, 2, 300, 130, 128, 2, "f16"),     # rows that see no key
+    inputs.Shape(2, 6, 3, 129, 257, 128, False, "bf16"),
+    inputs.Shape(1, 4, 4, 200, 150, 40, True, "bf16"),
+], ids=lambda s: s.name() if hasattr(s, "name") else str(s))
+def test_stage_entry_points(shape, det):
+    """fa_bwd_preprocess, fa_bwd_main and fa_bwd_dq called one at a time, on a workspace
+    filled with garbage and outputs filled with 7.0: the gradients must match the oracle,
+    and dK, dV (and, in deterministic mode, dQ) must equal fa_bwd's bit for bit."""
+    (q, k, v, do), _, _, g = oracle_full(shape, 11)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = torch_api.forward(qd, kd, vd, shape.softmax_scale, shape.causal)
+    B, Hq, Hkv, Nq, Nkv, d = shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nkv, shape.d
+    dt = _lib.FA_BF16 if shape.dtype == "bf16" else _lib.FA_F16
+    s = torch.cuda.current_stream()
+    ws = torch_api.workspace(qd, kd, det)
+    ws.fill_(0x7F)                                   # contents on entry must not matter
+    dq, dk, dv = torch.full_like(qd, 7.0), torch.full_like(kd, 7.0), torch.full_like(vd, 7.0)
+    c = int(shape.causal)
+    assert _lib.fa_bwd_preprocess(o, dod, lse, B, Hq, Hkv, Nq, Nkv, d, dt, det, ws, ws.numel(), s) == 0
+    assert _lib.fa_bwd_main(qd, kd, vd, dod, dk, dv, B, Hq, Hkv, Nq, Nkv, d, shape.softmax_scale, c, dt, det,
+                            ws, ws.numel(), s) == 0
+    assert _lib.fa_bwd_dq(qd, kd, vd, dod, dq, B, Hq, Hkv, Nq, Nkv, d, shape.softmax_scale, c, dt, det,
+                          ws, ws.numel(), s) == 0
+    torch.cuda.synchronize()
+    assert _lib.fa_last_device_error() == _lib.FA_OK
+    fails, rep = errors({"dQ": (_np(dq), g["dq"]), "dK": (_np(dk), g["dk"]), "dV": (_np(dv), g["dv"])})
+    assert not fails, rep
+    ref = torch_api.backward(qd, kd, vd, o, dod, lse, shape.softmax_scale, shape.causal, det)
+    torch.cuda.synchronize()
+    assert torch.equal(ref[1], dk) and torch.equal(ref[2], dv)
+    if det:
+        assert torch.equal(ref[0], dq)
+
+
 def test_deterministic_is_bitwise_reproducible():
     shape = inputs.llama_gqa(1000)
     q, k, v, do = (t.cuda() for t in inputs.draw(shape, 8))
