@@ -309,9 +309,10 @@ int run_fwd(const Geo& g, const void* q, const void* k, const void* v, void* o, 
   if ((st = fwd_abort_slot(&call_abort, &call_tag))) return st;
   CUtensorMap tq, tk, tv;
   const int bf = a.pb.bf16;
+  const int kv_rows = g.bias != nullptr ? kFwdBKBias : kFwdBK;
   if ((st = map_q(&tq, q, g.st.q, bf, g, 128))) return st;
-  if ((st = map_k(&tk, k, g.st.k, bf, g, 128))) return st;
-  if ((st = map_k(&tv, v, g.st.v, bf, g, 128))) return st;
+  if ((st = map_k(&tk, k, g.st.k, bf, g, kv_rows))) return st;
+  if ((st = map_k(&tv, v, g.st.v, bf, g, kv_rows))) return st;
   CUtensorMap tb{};
   if (g.bias != nullptr && (st = make_bias_map(&tb, g.bias, bf, g.Nkv, g.Nq, g.Hq, g.B, g.bias_st, 64, 128)))
     return st;

@@ -16,14 +16,18 @@
 // more than 8, which keeps P <= 256 and makes rescaling rare after the first
 // tiles.
 //
-// Warp roles (384 threads): warp 0 TMA producer (both query tiles once, a 2-stage K/V
-// ring they share), warp 1 owns TMEM and issues G1, warp 2 issues PV, and one
-// softmax warpgroup per query tile: thread r owns query row r (TMEM lane r) and all
-// 128 columns of each S tile.  TMEM: S_0, S_1, O_0, O_1.
-// With an additive bias the CTA takes one query tile (256 threads), and the freed
-// shared memory holds a 2-stage ring of [128 query x 128 key] bias tiles that the
-// producer loads by TMA next to K and V (128-byte swizzle, so that each thread
-// reads its own row in 16-byte pieces without bank conflicts).
+// Warp roles (384 threads): warp 0 TMA producer (both query tiles once, a 4-stage ring
+// of 64-key K/V tiles they share), warp 1 owns TMEM and issues G1, warp 2 issues PV,
+// and one softmax warpgroup per query tile: thread r owns query row r (TMEM lane r)
+// and all 64 columns of each S tile.  TMEM per query tile: two S buffers of 64
+// columns and O (128 columns), so S of the next KV tile is computed while the
+// softmax of the current one runs, and only S two tiles ahead waits for the P V
+// that reads the P packed into its buffer.
+// With an additive bias the CTA takes one query tile (256 threads) and steps over
+// 128 keys with one S buffer, and the freed shared memory holds a 2-stage ring of
+// [128 query x 128 key] bias tiles that the producer loads by TMA next to K and V
+// (128-byte swizzle, so that each thread reads its own row in 16-byte pieces without
+// bank conflicts).
 #include <cstdint>
 #include <climits>
 #include <math_constants.h>
@@ -36,44 +40,58 @@ namespace fa {
 namespace {
 
 constexpr int BQ = 128;     // query rows per tile (TMEM lanes)
-constexpr int BK = 128;     // KV rows per step
-constexpr int STAGES = 2;   // K/V ring depth (each K/V tile serves every query tile of the CTA)
 constexpr int BSTAGES = 2;  // bias ring depth
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 
-// query tiles per CTA (one softmax warpgroup each) and threads
+// Query tiles per CTA (one softmax warpgroup each), threads, keys per step, K/V ring
+// depth (each K/V tile serves every query tile of the CTA) and S buffers per query tile.
 template <bool BIAS>
 struct Cfg {
   static constexpr int NT = BIAS ? 1 : 2;
   static constexpr int kThreads = 128 + NT * 128;
+  static constexpr int BK = BIAS ? 128 : 64;
+  static constexpr int STAGES = BIAS ? 2 : 4;
+  static constexpr int SB = BIAS ? 1 : 2;
 };
 
 template <int D, bool BIAS>
 struct Layout {
   static constexpr int NT = Cfg<BIAS>::NT;
+  static constexpr int BK = Cfg<BIAS>::BK;
+  static constexpr int STAGES = Cfg<BIAS>::STAGES;
+  static constexpr int SB = Cfg<BIAS>::SB;
   static constexpr int NH = D / 64;
-  static constexpr int HALF = 128 * 128;        // one 64-column half of a 128-row tile
+  static constexpr int HALF = 128 * 128;        // one 64-column half of a 128-row query tile
   static constexpr int TILE = NH * HALF;
+  static constexpr int KHALF = BK * 128;        // one 64-column half of a K or V tile
+  static constexpr int KV_TILE = NH * KHALF;
   static constexpr int OFF_Q = 0;               // query tile x at OFF_Q + x*TILE
-  static constexpr int OFF_KV = NT * TILE;      // stage s: K at OFF_KV + 2*s*TILE, V after it
-  static constexpr int OFF_BIAS = OFF_KV + STAGES * 2 * TILE;
+  static constexpr int OFF_KV = NT * TILE;      // stage s: K at OFF_KV + 2*s*KV_TILE, V after it
+  static constexpr int OFF_BIAS = OFF_KV + STAGES * 2 * KV_TILE;
   static constexpr int BIAS_TILE = 2 * HALF;    // [128 query x 128 key], two 64-key halves
   static constexpr int OFF_BAR = OFF_BIAS + (BIAS ? BSTAGES * BIAS_TILE : 0);
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int TOTAL = OFF_MISC + 16;
   static constexpr int ALLOC = (TOTAL + 1024) > 120 * 1024 ? (TOTAL + 1024) : 120 * 1024;
-  static constexpr int COL_S = 0;               // S of query tile x at COL_S + x*BK
-  static constexpr int COL_O = NT * BK;         // O of query tile x at COL_O + x*128
-  static_assert(COL_O + (NT - 1) * 128 + D <= 512, "TMEM budget");
+  // TMEM of query tile x: its S buffers, then O
+  static constexpr int TCOLS = SB * BK + 128;
+  __host__ __device__ static constexpr int col_s(int x, int s) { return x * TCOLS + s * BK; }
+  __host__ __device__ static constexpr int col_o(int x) { return x * TCOLS + SB * BK; }
+  static_assert(NT * TCOLS <= 512 && D <= 128, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-enum : int {
-  B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_S = 1 + 2 * STAGES, B_P = B_S + 2, B_SFREE = B_P + 2,
-  B_PV = B_SFREE + 2, B_AFIN = B_PV + 2, B_BFULL, B_BEMPTY = B_BFULL + BSTAGES, B_END = B_BEMPTY + BSTAGES
+// Barriers.  Per query tile x and S buffer s (index 2x + s): S ready, P written, P read
+// by P V (the buffer may take a new S).  Per query tile: P V complete.
+template <bool BIAS>
+struct Bars {
+  static constexpr int ST = Cfg<BIAS>::STAGES;
+  static constexpr int Q = 0, KVFULL = 1, KVEMPTY = 1 + ST, S = 1 + 2 * ST, P = S + 4, SFREE = P + 4,
+                       PV = SFREE + 4, AFIN = PV + 2, BFULL = AFIN + 1, BEMPTY = BFULL + BSTAGES,
+                       END = BEMPTY + BSTAGES;
 };
-static_assert(B_END <= 24, "barrier count");
+static_assert(Bars<false>::END <= 32 && Bars<true>::END <= 32, "barrier count");
 
 struct Params {
   void* o;
@@ -99,7 +117,11 @@ __global__ void __launch_bounds__(Cfg<BIAS>::kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias, const Params p) {
   using L = Layout<D, BIAS>;
+  using Br = Bars<BIAS>;
   constexpr int NT = L::NT;
+  constexpr int BK = L::BK;
+  constexpr int STAGES = L::STAGES;
+  constexpr int SB = L::SB;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled tiles.  Offsetting the array itself
   // (not a rounded integer) keeps the pointer in the shared address space, so
@@ -140,21 +162,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   for (int x = 0; x < NT; ++x) T = max(T, Tx[x]);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_Q), 1);
+    mbar_init(bar(Br::Q), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_KVFULL + s), 1);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+      mbar_init(bar(Br::KVFULL + s), 1);
+      mbar_init(bar(Br::KVEMPTY + s), 1);
     }
     for (int x = 0; x < NT; ++x) {        // per query tile
-      mbar_init(bar(B_S + x), 1);
-      mbar_init(bar(B_P + x), 4);       // one arrival per softmax warp
-      mbar_init(bar(B_SFREE + x), 1);
-      mbar_init(bar(B_PV + x), 1);
+      for (int s = 0; s < SB; ++s) {      // and S buffer
+        mbar_init(bar(Br::S + 2 * x + s), 1);
+        mbar_init(bar(Br::P + 2 * x + s), 4);   // one arrival per softmax warp
+        mbar_init(bar(Br::SFREE + 2 * x + s), 1);
+      }
+      mbar_init(bar(Br::PV + x), 1);
     }
-    mbar_init(bar(B_AFIN), 1);
+    mbar_init(bar(Br::AFIN), 1);
     for (int i = 0; i < BSTAGES; ++i) {
-      mbar_init(bar(B_BFULL + i), 1);
-      mbar_init(bar(B_BEMPTY + i), 4);  // one arrival per softmax warp
+      mbar_init(bar(Br::BFULL + i), 1);
+      mbar_init(bar(Br::BEMPTY + i), 4);  // one arrival per softmax warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -173,12 +197,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ================================================================ TMA producer
     if (lane == 0 && T > 0 &&
         FA_BOUNDS(h < p.Hq && bc < batch_extent(p.m) && sq.q_start + q0 < rows_q(p.m), wc, 80)) {
-      mbar_arrive_expect_tx(bar(B_Q), NT * L::TILE);
+      mbar_arrive_expect_tx(bar(Br::Q), NT * L::TILE);
 #pragma unroll
       for (int x = 0; x < NT; ++x)
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh)
-          tma_load_4d(sb + L::OFF_Q + x * L::TILE + hh * L::HALF, &tm_q, bar(B_Q), 64 * hh,
+          tma_load_4d(sb + L::OFF_Q + x * L::TILE + hh * L::HALF, &tm_q, bar(Br::Q), 64 * hh,
                       sq.q_start + q0 + x * BQ, h, bc);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -187,21 +211,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (!FA_BOUNDS(sq.k_start + t * BK < rows_k(p.m) && hk < p.Hkv, wc, 81)) break;
         if constexpr (BIAS)
           if (!FA_BOUNDS(t * BK < p.Nkv && (p.m.bias_st.n == 0 || q0 < p.Nq) && h < p.Hq && b < p.B, wc, 82)) break;
-        if (t >= STAGES && !mbar_wait(bar(B_KVEMPTY + s), ph ^ 1, wc, 51)) break;
-        const uint32_t fb = bar(B_KVFULL + s);
-        mbar_arrive_expect_tx(fb, 2 * L::TILE);
-        const uint32_t dst = sb + L::OFF_KV + s * 2 * L::TILE;
+        if (t >= STAGES && !mbar_wait(bar(Br::KVEMPTY + s), ph ^ 1, wc, 51)) break;
+        const uint32_t fb = bar(Br::KVFULL + s);
+        mbar_arrive_expect_tx(fb, 2 * L::KV_TILE);
+        const uint32_t dst = sb + L::OFF_KV + s * 2 * L::KV_TILE;
 #pragma unroll
         for (int hh = 0; hh < L::NH; ++hh) {
-          tma_load_4d(dst + hh * L::HALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
-          tma_load_4d(dst + L::TILE + hh * L::HALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
+          tma_load_4d(dst + hh * L::KHALF, &tm_k, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
+          tma_load_4d(dst + L::KV_TILE + hh * L::KHALF, &tm_v, fb, 64 * hh, sq.k_start + t * BK, hk, bc);
         }
         if constexpr (BIAS) {
           // bias of (query rows q0.., keys t*BK..) of head h, sequence b; a broadcast
           // axis has extent 1 in the map and is addressed at 0
           const int bs = t & (BSTAGES - 1);
-          if (t >= BSTAGES && !mbar_wait(bar(B_BEMPTY + bs), ((t / BSTAGES) & 1) ^ 1, wc, 59)) break;
-          const uint32_t bb = bar(B_BFULL + bs);
+          if (t >= BSTAGES && !mbar_wait(bar(Br::BEMPTY + bs), ((t / BSTAGES) & 1) ^ 1, wc, 59)) break;
+          const uint32_t bb = bar(Br::BFULL + bs);
           mbar_arrive_expect_tx(bb, L::BIAS_TILE);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
@@ -210,71 +234,76 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         issued = t + 1;
       }
-      drain_wait(bar(B_Q), 0);
+      drain_wait(bar(Br::Q), 0);
       for (int t = max(0, issued - STAGES); t < issued; ++t)
-        drain_wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1);
+        drain_wait(bar(Br::KVFULL + t % STAGES), (t / STAGES) & 1);
       if constexpr (BIAS)
         for (int t = max(0, issued - BSTAGES); t < issued; ++t)
-          drain_wait(bar(B_BFULL + (t & (BSTAGES - 1))), (t / BSTAGES) & 1);
+          drain_wait(bar(Br::BFULL + (t & (BSTAGES - 1))), (t / BSTAGES) & 1);
     }
   } else if (warp == 1 || warp == 2) {
     // ================================================================ MMA issuers
     if (T > 0) {
       constexpr uint32_t ID_S = make_idesc_f16(128, BK, BF16, false, false);
       constexpr uint32_t ID_O = make_idesc_f16(128, D, BF16, false, true);
-      auto s_buf = [&](int x) -> uint32_t { return tmem + L::COL_S + x * BK; };
-      auto o_buf = [&](int x) -> uint32_t { return tmem + L::COL_O + x * 128; };
-      auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_KV + (t % STAGES) * 2 * L::TILE; };
-      auto kstep = [](int ks) -> uint64_t {
-        return static_cast<uint64_t>(((ks >> 2) * L::HALF + (ks & 3) * 32) >> 4);
+      auto s_buf = [&](int x, int t) -> uint32_t { return tmem + L::col_s(x, t % SB); };
+      auto o_buf = [&](int x) -> uint32_t { return tmem + L::col_o(x); };
+      auto k_tile = [&](int t) -> uint32_t { return sb + L::OFF_KV + (t % STAGES) * 2 * L::KV_TILE; };
+      // descriptor advance of k-step ks (16 columns of d) in a K-major tile of 64-column
+      // halves of `half` bytes
+      auto kstep = [](int ks, int half) -> uint64_t {
+        return static_cast<uint64_t>(((ks >> 2) * half + (ks & 3) * 32) >> 4);
       };
       auto wait = [&](uint32_t bb, uint32_t parity, uint32_t site) -> bool {
         return __all_sync(0xffffffffu, mbar_wait(bb, parity, wc, site));
       };
       if (warp == 1) {
-        // G1: S_x = Q_x K^T for both query tiles, each once P V of its previous
-        // tile has read the P that sits in its S columns
-        bool ok = wait(bar(B_Q), 0, 52);
+        // G1: S_x(t) = Q_x K(t)^T for both query tiles into S buffer t mod SB of tile x,
+        // once P V of KV tile t - SB has read the P that sits in that buffer
+        bool ok = wait(bar(Br::Q), 0, 52);
         for (int t = 0; ok && t < T; ++t) {
-          if (!wait(bar(B_KVFULL + t % STAGES), (t / STAGES) & 1, 53)) break;
+          if (!wait(bar(Br::KVFULL + t % STAGES), (t / STAGES) & 1, 53)) break;
           const uint64_t dK_k = sw128_desc(k_tile(t), 16, 1024);
+          const int sbi = t % SB;
 #pragma unroll
           for (int x = 0; x < NT; ++x) {
             if (t >= Tx[x]) continue;
-            if (t >= 1 && !wait(bar(B_SFREE + x), (t - 1) & 1, 54)) { ok = false; break; }
+            if (t >= SB && !wait(bar(Br::SFREE + 2 * x + sbi), ((t - SB) / SB) & 1, 54)) { ok = false; break; }
             tc_fence_after();
             const uint64_t dQ_k = sw128_desc(sb + L::OFF_Q + x * L::TILE, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              umma_ss_warp(s_buf(x), dQ_k + kstep(ks), dK_k + kstep(ks), ID_S, ks > 0);
-            umma_commit_warp(bar(B_S + x));
+              umma_ss_warp(s_buf(x, t), dQ_k + kstep(ks, L::HALF), dK_k + kstep(ks, L::KHALF), ID_S, ks > 0);
+            umma_commit_warp(bar(Br::S + 2 * x + sbi));
           }
         }
-        umma_commit_warp(bar(B_AFIN));
-        drain_wait(bar(B_AFIN), 0);
+        umma_commit_warp(bar(Br::AFIN));
+        drain_wait(bar(Br::AFIN), 0);
       } else {
-        // PV: O_x += P_x V (P, 16-bit, packed into the first half of S_x; V read MN-major)
+        // PV: O_x += P_x(t) V(t) (P, 16-bit, packed into the first half of its S buffer;
+        // V read MN-major)
         bool ok = true;
         for (int t = 0; ok && t < T; ++t) {
-          const uint64_t dV_mn = sw128_desc(k_tile(t) + L::TILE, L::HALF, 1024);
+          const uint64_t dV_mn = sw128_desc(k_tile(t) + L::KV_TILE, L::KHALF, 1024);
+          const int sbi = t % SB;
 #pragma unroll
           for (int x = 0; x < NT; ++x) {
             if (t >= Tx[x]) continue;
-            if (!wait(bar(B_P + x), t & 1, 55)) { ok = false; break; }
+            if (!wait(bar(Br::P + 2 * x + sbi), (t / SB) & 1, 55)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < BK / 16; ++ks)
-              umma_ts_warp(o_buf(x), s_buf(x) + 8 * ks, dV_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_O,
+              umma_ts_warp(o_buf(x), s_buf(x, t) + 8 * ks, dV_mn + static_cast<uint64_t>((ks * 2048) >> 4), ID_O,
                            (t > 0 || ks > 0));
-            umma_commit_warp(bar(B_SFREE + x));
-            umma_commit_warp(bar(B_PV + x));
+            umma_commit_warp(bar(Br::SFREE + 2 * x + sbi));
+            umma_commit_warp(bar(Br::PV + x));
           }
           if (!ok) break;
-          umma_commit_warp(bar(B_KVEMPTY + t % STAGES));   // every G1(t) completed before its P(t) existed
+          umma_commit_warp(bar(Br::KVEMPTY + t % STAGES));   // every G1(t) completed before its P(t) existed
         }
         if (*abort_flag)
           for (int x = 0; x < NT; ++x)
-            if (Tx[x] > 0) drain_wait(bar(B_PV + x), (Tx[x] - 1) & 1);
+            for (int t = max(0, min(Tx[x], T) - SB); t < Tx[x]; ++t) drain_wait(bar(Br::PV + x), t & 1);
       }
     }
   } else if (warp >= 4) {
@@ -282,7 +311,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int qt = (warp - 4) >> 2;                     // query tile of this warpgroup
     const int r = threadIdx.x - 128 - 128 * qt;         // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_off + L::COL_O + qt * 128;
+    const uint32_t tO = tmem + lane_off + L::col_o(qt);
     const int q = q0 + qt * BQ + r;
     const int T = Tx[qt];
     // this thread's row of a staged bias tile (row 0 when the bias broadcasts over queries)
@@ -297,13 +326,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       int lim = sq.nk - kv0;
       if (p.causal) lim = min(lim, q + sq.delta - kv0 + 1);
       const bool need_mask = __any_sync(0xffffffffu, lim < BK);
-      const uint32_t tS = tmem + lane_off + L::COL_S + qt * BK;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + qt), t & 1, wc, 56))) { ok = false; break; }
+      const int sbi = t % SB;
+      const uint32_t tS = tmem + lane_off + L::col_s(qt, sbi);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(Br::S + 2 * qt + sbi), (t / SB) & 1, wc, 56))) { ok = false; break; }
       tc_fence_after();
       float x[BK];
       if constexpr (BIAS) {
         const int bs = t & (BSTAGES - 1);
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_BFULL + bs), (t / BSTAGES) & 1, wc, 60))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(Br::BFULL + bs), (t / BSTAGES) & 1, wc, 60))) { ok = false; break; }
         const uint8_t* btile = smem + L::OFF_BIAS + bs * L::BIAS_TILE + brow * 128;
 #pragma unroll
         for (int ch = 0; ch < BK / 32; ++ch) {
@@ -330,7 +360,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             x[32 * ch + c] = fmaf(bv[c], 1.4426950408889634f, __uint_as_float(sr[c]) * p.scale_log2);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_BEMPTY + bs));   // this warp's bias reads are done
+        if (lane == 0) mbar_arrive(bar(Br::BEMPTY + bs));   // this warp's bias reads are done
       } else {
         // all four 32-column loads in flight at once, one wait
         uint32_t sr[BK];
@@ -364,7 +394,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const bool resc = !first && mt > m_ref + kRescaleThreshold;
         if (first) m_ref = mt;
         if (__any_sync(0xffffffffu, resc)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV + qt), (t - 1) & 1, wc, 57))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (t - 1) & 1, wc, 57))) { ok = false; break; }
           tc_fence_after();
           const float alpha = resc ? ex2_approx(m_ref - mt) : 1.f;
 #pragma unroll 1
@@ -406,12 +436,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P + qt));
+      if (lane == 0) mbar_arrive(bar(Br::P + 2 * qt + sbi));
     }
     // ---- epilogue: O = acc / l (16-bit), L = (m_ref + log2 l) * ln 2
     bool have = ok && T > 0;
     if (have) {
-      have = __all_sync(0xffffffffu, mbar_wait(bar(B_PV + qt), (T - 1) & 1, wc, 58));
+      // With two S buffers both of the last two P V may still be running, and a parity
+      // wait tells only the current phase from the previous one: wait for them in order.
+      if (SB > 1 && T > 1) have = __all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (T - 2) & 1, wc, 49));
+      if (have) have = __all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (T - 1) & 1, wc, 58));
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0 || !(q < sq.nq ? FA_BOUNDS(sq.q_start + q < rows_q(p.m), wc, 83) : true);
@@ -470,6 +503,7 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
   p.causal = a.pb.causal;
   p.m = seq_map(a.pb);
   const long long grid = static_cast<long long>(((a.pb.Nq + BQ - 1) / BQ + NT - 1) / NT) * a.pb.B * a.pb.Hq;
+  static_assert(Cfg<BIAS>::BK == (BIAS ? kFwdBKBias : kFwdBK), "K/V tensor-map box rows");
   kern<<<static_cast<unsigned>(grid), Cfg<BIAS>::kThreads, L::ALLOC, stream>>>(tq, tk, tv, tb, p);
   return cudaGetLastError();
 }

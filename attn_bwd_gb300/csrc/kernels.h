@@ -17,6 +17,10 @@ constexpr int kRowPad = 128;
 constexpr int kMainBN = 128;
 constexpr int kMainBM = 64;
 
+// Keys per step of the forward kernel: the box height of its K and V tensor maps.
+constexpr int kFwdBK = 64;        // no bias
+constexpr int kFwdBKBias = 128;   // with an additive bias
+
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // SM count of the current device (1 if it cannot be read).
@@ -152,8 +156,9 @@ cudaError_t launch_bwd_main_persist(const MainArgs& a, const CUtensorMap& tq, co
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
-// fwd.cu: maps are Q, K, V (box 64 x 128 rows) and the bias (box 64 keys x 128 queries,
-// 128-byte swizzle; used only when the problem has a bias)
+// fwd.cu: maps are Q (box 64 x 128 rows), K, V (box 64 x kFwdBK rows, or kFwdBKBias with a
+// bias) and the bias (box 64 keys x 128 queries, 128-byte swizzle; used only when the
+// problem has a bias)
 // `call_abort` is the call's abort word (a slot of a ring) and `call_tag` the value the
 // call stores there when it gives up; no earlier user of the slot had that tag.
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
