@@ -45,8 +45,9 @@ preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO, con
   constexpr int RPB = 256 / TPR;             // rows per block per sweep
   const int sub = threadIdx.x % TPR;
   // the later kernels of this call start with a clear abort word (word 0 of the workspace
-  // header) and item counters (words 1, 2: the persistent main kernel's)
-  if (blockIdx.x == 0 && threadIdx.x < 3) call_abort[threadIdx.x] = 0u;
+  // header) and item counters (words 1, 2: the persistent main kernel's; 3, 4: the
+  // persistent deterministic dQ kernel's)
+  if (blockIdx.x == 0 && threadIdx.x < 5) call_abort[threadIdx.x] = 0u;
   // The sweep base is block-uniform so every lane reaches the row shuffle below.
   for (long long base = static_cast<long long>(blockIdx.x) * RPB; base < rows;
        base += static_cast<long long>(gridDim.x) * RPB) {

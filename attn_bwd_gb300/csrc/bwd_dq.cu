@@ -1,4 +1,6 @@
-// bwd_dq.cu -- deterministic dQ pass on tcgen05 tensor cores.
+// bwd_dq.cu -- deterministic dQ pass on tcgen05 tensor cores, one CTA per work
+// item (the form that serves problems with an additive bias; bwd_dq_persist.cu
+// runs the same products persistently for every other problem).
 //
 // One CTA owns a 128-row query tile of one query head and walks the KV tiles
 // it can see in a fixed order, keeping dQ in TMEM, so the summation order of
@@ -402,6 +404,7 @@ cudaError_t launch_t(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& 
 
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  if (use_persistent(a.pb)) return launch_bwd_dq_persist(a, tq, tdo, tk, tv, stream);
   const bool bias = a.pb.bias != nullptr;
   if (a.pb.d > 64) {
     if (a.pb.bf16)

@@ -36,7 +36,8 @@ inline int sm_count() {
 struct Workspace {
   unsigned int* abort;   // the call's abort word (first 256 bytes): zeroed by the preprocess
                          // kernel, set by the first CTA of the main or dQ kernel that gives up;
-                         // words 1 and 2 are the persistent main kernel's item counters
+                         // words 1, 2 are the persistent main kernel's item counters, words 3, 4
+                         // the persistent deterministic dQ kernel's
   float* nLg;     // [B*Hq*NqPad]   -L * log2(e); -inf on padding rows
   float* Dv;      // [B*Hq*NqPad]   rowsum(dO o O); 0 on padding rows
   float* dq_acc;  // [B*Hq*NqPad*d] fp32 dQ accumulator (atomic mode only)
@@ -153,6 +154,10 @@ cudaError_t launch_bwd_main_persist(const MainArgs& a, const CUtensorMap& tq, co
                                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
 // bwd_dq.cu: maps are Q, dO (box 64 x 128 rows), K, V (box 64 x 128 rows)
+// bwd_dq_persist.cu: the deterministic dQ pass as a persistent kernel (problems without a bias;
+// launch_bwd_dq_det dispatches to it)
+cudaError_t launch_bwd_dq_persist(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
+                                  const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUtensorMap& tdo,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
