@@ -18,9 +18,11 @@
 //   - K and V of the next item are loaded (by a warp of their own) as soon as
 //     the current item's last products have read them, or, for d <= 64, where
 //     two K/V buffers fit next to the ring, while the current item is computed;
-//   - the softmax warps write an item's dK/dV while the MMA warps already
-//     compute S^T and dP^T of the next item; the next item's first dV/dK
-//     product waits only for that read-out.
+//   - the dQ warps (idle between their reductions, and in deterministic mode
+//     altogether) read an item's dV, then dK, out of TMEM and store them,
+//     while the softmax warps already work on the next item's first tiles;
+//     the next item's first dV (dK) product waits only for the dV (dK)
+//     read-out.
 // With short items (a 256-token head walks 4 query tiles per KV tile) the
 // set-up, load latency and epilogue of every item weigh on its time as much as
 // its tiles.  The item numbers reach the CTA's roles through a ring of eight
@@ -79,7 +81,7 @@ struct PLayout {
 // KVFULL, KVEMPTY one per K/V buffer (item n uses n % KVBUF)
 enum : int {
   KVFULL = 0, KVEMPTY = 2, QFULL = 4, QEMPTY = QFULL + QST, S = QEMPTY + QST, P = S + 2, SFREE = P + 2,
-  DP = SFREE + 2, DPFREE, DS, DQFULL, DQEMPTY, DSFREE, ACC, ACCFREE, AFIN1, AFIN2,
+  DP = SFREE + 2, DPFREE, DS, DQFULL, DQEMPTY, DSFREE, ACC, ACCFREE_V, ACCFREE_K, AFIN1, AFIN2,
   ITEM_FULL, ITEM_EMPTY = ITEM_FULL + 8, BAR_END = ITEM_EMPTY + 8
 };
 static_assert(BAR_END <= PLayout<128>::NBAR, "barrier count");
@@ -185,12 +187,13 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     mbar_init(bar(DQEMPTY), 4);        // one arrival per dQ warp
     mbar_init(bar(DSFREE), 1);
     mbar_init(bar(ACC), 1);
-    mbar_init(bar(ACCFREE), 8);        // the item's dK/dV read out of TMEM: one arrival per epilogue warp
+    mbar_init(bar(ACCFREE_V), 4);      // the item's dV read out of TMEM: one arrival per epilogue warp
+    mbar_init(bar(ACCFREE_K), 4);      // its dK
     mbar_init(bar(AFIN1), 1);          // warp 1's products have completed (at exit)
     mbar_init(bar(AFIN2), 1);          // warp 2's
     for (int i = 0; i < 8; ++i) {      // item ring: slot written / read by every other role's warp
       mbar_init(bar(ITEM_FULL + i), 1);
-      mbar_init(bar(ITEM_EMPTY + i), DET ? 11 : 15);
+      mbar_init(bar(ITEM_EMPTY + i), 15);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -381,8 +384,8 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const int kb = n % L::KVBUF;
         const uint64_t dK_mn = sw128_desc(sb + L::OFF_KV + 2 * kb * L::KV_BYTES, L::KHALF, 1024);
         for (int t = 0; t < w.T; ++t, ++g) {
-          // the item's first products start new dK/dV sums: the previous item's must have been read out
-          if (t == 0 && n >= 1 && !wait(bar(ACCFREE), (n - 1) & 1, 16)) { ok = false; break; }
+          // the item's first products start new dV/dK sums: the previous item's must have been read out
+          if (t == 0 && n >= 1 && !wait(bar(ACCFREE_V), (n - 1) & 1, 16)) { ok = false; break; }
           // G3: dV += P^T dO
           if (!wait(bar(P + (g & 1)), (g >> 1) & 1, 4)) { ok = false; break; }
           tc_fence_after();
@@ -394,6 +397,7 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             umma_commit_warp(bar(SFREE + (g & 1)));
           }
           // G4: dK += dS^T Q
+          if (t == 0 && n >= 1 && !wait(bar(ACCFREE_K), (n - 1) & 1, 12)) { ok = false; break; }
           if (!wait(bar(DS), g & 1, 5)) { ok = false; break; }
           tc_fence_after();
           {
@@ -426,18 +430,14 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       drain_wait(bar(AFIN2), 0);
     }
   } else if (warp >= 4 && warp < 12) {
-    // ================================================================ softmax / dS groups, epilogue
+    // ================================================================ softmax / dS groups
     const int grp = (warp - 4) >> 2;                      // query columns [32 grp, 32 grp + 32)
     const int r = threadIdx.x - 128 - 128 * grp;          // KV row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tdP = tmem + lane_off + L::COL_DP + 32 * grp;
     uint8_t* ds_row = smem + L::OFF_DS + r * 128;
     const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
-    // epilogue role: group 0 writes dK (x scale), group 1 writes dV
-    const bool is_dk = grp == 0;
-    const uint32_t tacc = tmem + lane_off + (is_dk ? L::COL_DK : L::COL_DV);
-    const float mul = is_dk ? p.scale : 1.0f;
-    int n = 0, g = 0;
+    int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int it = take_item(k);
@@ -445,17 +445,7 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const Item w = decode(it, p, G);
       const int kv = w.kv0 + r;
       const bool row_ok = kv < w.sq.nk;
-      uint8_t* out = reinterpret_cast<uint8_t*>(is_dk ? p.dk : p.dv) +
-                     at(is_dk ? p.m.st.dk : p.m.st.dv, p.m, w.b, w.hkv, w.sq.k_start + kv) * 2;
-      if (w.T == 0) {
-        // keys no query sees: dK = dV = 0
-        uint32_t zero[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) zero[c] = 0u;
-        if (row_ok && FA_BOUNDS(w.sq.k_start + kv < rows_k(p.m), wc, 69))
-          for (int ch = 0; ch < D / 32; ++ch) store_row_chunk<BF16>(out + ch * 64, zero, p.m.d - 32 * ch);
-        continue;
-      }
+      if (w.T == 0) continue;
       int qi = w.i0, h = w.hkv * G;
       for (int t = 0; t < w.T; ++t, ++g, h += (qi + 1 == w.nQt), qi = (qi + 1 == w.nQt) ? w.i0 : qi + 1) {
         const int s = g % QST;
@@ -537,40 +527,38 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (lane == 0) mbar_arrive(bar(DS));
       }
       if (!ok) break;
-      // ---- epilogue of the item: dK (x scale) or dV of KV row r, then release the accumulator
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(ACC), n & 1, wc, 13))) break;
-      tc_fence_after();
-      const bool aborted = *abort_flag != 0;
-      const bool store = row_ok && !aborted && FA_BOUNDS(w.sq.k_start + kv < rows_k(p.m), wc, 65);
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld_x32(tacc + ch * 32, v);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[c] = pack2<BF16>(__uint_as_float(v[2 * c]) * mul, __uint_as_float(v[2 * c + 1]) * mul);
-        if (store) store_row_chunk<BF16>(out + ch * 64, pk, p.m.d - 32 * ch);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(ACCFREE));
-      ++n;
     }
   } else if (warp >= 12) {
-    // ================================================================ dQ group
-    if constexpr (!DET) {
-      const int r = threadIdx.x - 384;                     // TMEM lane == column of dQ
-      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t tdQ = tmem + lane_off + L::COL_DQ;
-      int g = 0;
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int it = take_item(k);
-        if (it < 0) break;
-        const Item w = decode(it, p, G);
-        if (w.T == 0) continue;
+    // ================================================================ dQ group, epilogue
+    // Per tile (atomic mode): dQ^T from TMEM into the fp32 accumulator.  Per item: dK
+    // (x scale) and dV of KV row r out of TMEM, release of the accumulators, then the
+    // stores, while the softmax warps already work on the next item's first tiles.
+    const int r = threadIdx.x - 384;                     // TMEM lane: dQ column, KV row of dK/dV
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tdQ = tmem + lane_off + L::COL_DQ;
+    int n = 0, g = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int it = take_item(k);
+      if (it < 0) break;
+      const Item w = decode(it, p, G);
+      const int kv = w.kv0 + r;
+      const bool row_ok = kv < w.sq.nk && FA_BOUNDS(w.sq.k_start + kv < rows_k(p.m), wc, 65);
+      uint8_t* out_k = reinterpret_cast<uint8_t*>(p.dk) + at(p.m.st.dk, p.m, w.b, w.hkv, w.sq.k_start + kv) * 2;
+      uint8_t* out_v = reinterpret_cast<uint8_t*>(p.dv) + at(p.m.st.dv, p.m, w.b, w.hkv, w.sq.k_start + kv) * 2;
+      if (w.T == 0) {
+        // keys no query sees: dK = dV = 0
+        uint32_t zero[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) zero[c] = 0u;
+        if (row_ok)
+          for (int ch = 0; ch < D / 32; ++ch) {
+            store_row_chunk<BF16>(out_k + ch * 64, zero, p.m.d - 32 * ch);
+            store_row_chunk<BF16>(out_v + ch * 64, zero, p.m.d - 32 * ch);
+          }
+        continue;
+      }
+      if constexpr (!DET) {
         int h = w.hkv * G, qi = w.i0;
         for (int t = 0; t < w.T; ++t, ++g) {
           const int q0 = qi * BM;
@@ -597,7 +585,39 @@ bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             ++h;
           }
         }
+        if (!ok) break;
       }
+      // ---- epilogue of the item: dV, then dK (x scale), of KV row r: each read out of TMEM
+      // into 16-bit, released for the next item's first product into it, then stored
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(ACC), n & 1, wc, 13))) break;
+      tc_fence_after();
+      const bool store = row_ok && *abort_flag == 0;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tacc = tmem + lane_off + (which == 0 ? L::COL_DV : L::COL_DK);
+        const float mul = which == 0 ? 1.0f : p.scale;
+        uint32_t pk[D / 2];
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t a[32];
+          tmem_ld_x32(tacc + ch * 32, a);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[16 * ch + c] = pack2<BF16>(__uint_as_float(a[2 * c]) * mul, __uint_as_float(a[2 * c + 1]) * mul);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(which == 0 ? ACCFREE_V : ACCFREE_K));
+        if (store) {
+          uint8_t* out = which == 0 ? out_v : out_k;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch)
+            store_row_chunk<BF16>(out + ch * 64, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * ch),
+                                  p.m.d - 32 * ch);
+        }
+      }
+      ++n;
     }
   }
 
