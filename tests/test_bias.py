@@ -122,3 +122,24 @@ def test_bias_on_packed_batch(causal, det):
                 f"dV[{b}]": (_np(dv[:, sl_k][None]), r["dv"]),
                 f"dBias[{b}]": (_np(dbh[b:b + 1, :, :nq, :nk]), r["dbias"])})
     assert (dbh[untouched] == sentinel).all(), "dBias written outside a sequence"
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_zero_bias_gives_the_same_bits(causal):
+    """A zero bias adds exactly 0 to every exponent, so the backward's bias path (one CTA per
+    work item) and its path without a bias (persistent kernels) must compute the same bits from
+    the same O and L: dK and dV in both dQ modes, and the deterministic dQ, whose summation
+    order both fix the same way.  (The forward is not compared: with a bias it steps over 128
+    keys at a time instead of 64, which moves its running maxima.)"""
+    shape = inputs.Shape(2, 4, 2, 300, 264, 128, causal, "bf16")   # bias rows need 16-byte strides
+    q, k, v, do = (t.cuda() for t in inputs.draw(shape, 72))
+    zero = torch.zeros(1, 1, 300, 264, dtype=torch.bfloat16, device="cuda")
+    o, lse = torch_api.forward(q, k, v, shape.softmax_scale, causal)
+    for det in (False, True):
+        g0 = torch_api.backward(q, k, v, o, do, lse, shape.softmax_scale, causal, det)
+        g1 = torch_api.backward_bias(q, k, v, o, do, lse, zero, shape.softmax_scale, causal, det)
+        torch.cuda.synchronize()
+        assert _lib.fa_last_device_error() == _lib.FA_OK
+        assert torch.equal(g0[1], g1[1]) and torch.equal(g0[2], g1[2]), f"dK/dV det={det}"
+        if det:
+            assert torch.equal(g0[0], g1[0]), "deterministic dQ"
