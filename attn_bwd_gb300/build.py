@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libattn_bwd_gb300.so")
 LIB_BOUNDS = os.path.join(PKG, "libattn_bwd_gb300_bounds.so")
 SOURCES = ["api.cu", "bwd_main.cu", "bwd_main_persist.cu", "bwd_dq.cu", "bwd_dq_persist.cu", "bwd_aux.cu", "fwd.cu",
-           "noalloc.cu", "host_pipeline.cu"]
+           "fwd_persist.cu", "noalloc.cu", "host_pipeline.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", "seq.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]

@@ -1,4 +1,6 @@
-// fwd.cu -- exact attention forward on tcgen05 tensor cores, producing O and
+// fwd.cu -- exact attention forward on tcgen05 tensor cores, one CTA per work item
+// (launched for problems with a bias; without one, fwd_persist.cu runs this kernel's
+// no-bias configuration persistently), producing O and
 // the log-sum-exp L that the backward consumes (L is the natural-log LSE of the
 // scaled, masked scores: the convention of flash_attention_backward.cu,
 // rustytorch rtx-flash-attention, block "Compute softmax probabilities from
@@ -434,6 +436,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_st_wait();
+      // With two S buffers, the previous P V must have completed before the last P goes out:
+      // the epilogue would otherwise have two P V to wait for, and once both have completed, a
+      // parity wait for the older one would wait for a phase two ahead.  Here at most that one
+      // P V is outstanding.
+      if (SB > 1 && t == T - 1 && T > 1 &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (t - 1) & 1, wc, 49))) {
+        ok = false;
+        break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Br::P + 2 * qt + sbi));
@@ -441,10 +452,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ---- epilogue: O = acc / l (16-bit), L = (m_ref + log2 l) * ln 2
     bool have = ok && T > 0;
     if (have) {
-      // With two S buffers both of the last two P V may still be running, and a parity
-      // wait tells only the current phase from the previous one: wait for them in order.
-      if (SB > 1 && T > 1) have = __all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (T - 2) & 1, wc, 49));
-      if (have) have = __all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (T - 1) & 1, wc, 58));
+      // the last P V is the only one still outstanding (see the last tile's step above)
+      have = __all_sync(0xffffffffu, mbar_wait(bar(Br::PV + qt), (T - 1) & 1, wc, 58));
       tc_fence_after();
     }
     const bool aborted = *abort_flag != 0 || !(q < sq.nq ? FA_BOUNDS(sq.q_start + q < rows_q(p.m), wc, 83) : true);
@@ -513,19 +522,13 @@ cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort,
                        unsigned int call_tag, cudaStream_t stream) {
-  const bool bias = a.pb.bias != nullptr;
-  if (a.pb.d > 64) {
-    if (a.pb.bf16)
-      return bias ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
-                  : launch_t<128, true, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
-    return bias ? launch_t<128, false, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
-                : launch_t<128, false, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
-  }
-  if (a.pb.bf16)
-    return bias ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
-                : launch_t<64, true, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
-  return bias ? launch_t<64, false, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
-              : launch_t<64, false, false>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
+  // without a bias: the persistent form of this kernel's no-bias configuration
+  if (a.pb.bias == nullptr) return launch_fwd_persist(a, tq, tk, tv, status, call_abort, call_tag, stream);
+  if (a.pb.d > 64)
+    return a.pb.bf16 ? launch_t<128, true, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
+                     : launch_t<128, false, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
+  return a.pb.bf16 ? launch_t<64, true, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream)
+                   : launch_t<64, false, true>(a, tq, tk, tv, tb, status, call_abort, call_tag, stream);
 }
 
 }  // namespace fa

@@ -169,5 +169,10 @@ cudaError_t launch_bwd_dq_det(const DqArgs& a, const CUtensorMap& tq, const CUte
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, unsigned int* status, unsigned int* call_abort,
                        unsigned int call_tag, cudaStream_t stream);
+// fwd_persist.cu: the forward as a persistent kernel (problems without a bias; launch_fwd
+// dispatches to it)
+cudaError_t launch_fwd_persist(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               unsigned int* status, unsigned int* call_abort, unsigned int call_tag,
+                               cudaStream_t stream);
 
 }  // namespace fa

@@ -435,7 +435,7 @@ def main():
                 "api": f"fa_bwd_host (pinned host tensors, transfers overlapped in chunks of {chunk_groups} "
                        f"(batch, kv-head) groups through {slots} staging slots)"},
         "gpu_launches": 3 * args.steps,
-        "forward": {"kernel": "fwd_kernel (makes O and L; outside the timed step)", "ms": fwd_ms,
+        "forward": {"kernel": "fwd_persist_kernel (makes O and L; outside the timed step)", "ms": fwd_ms,
                     "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
                     "frac": fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak,
                     "flops": "4*B*Hq*Nq*Nkv*d, halved for causal"},

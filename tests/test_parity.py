@@ -226,6 +226,27 @@ def test_stage_entry_points(shape, det):
         assert torch.equal(ref[0], dq)
 
 
+@pytest.mark.parametrize("det", [False, True], ids=["atomic", "deterministic"])
+def test_workspace_reused_across_calls(det):
+    """The persistent kernels hand out work items from counters in the workspace header and the
+    last CTA of each launch resets them (and the preprocess kernel of each call clears them).
+    One workspace, sized for the largest problem, serves several calls of different shapes and
+    causal modes in a row; each result must match the oracle."""
+    shapes = [inputs.Shape(1, 8, 2, 512, 512, 128, True, "bf16"), inputs.Shape(2, 4, 4, 200, 77, 64, 2, "f16"),
+              inputs.Shape(1, 4, 1, 333, 333, 128, False, "bf16"), inputs.Shape(1, 8, 2, 512, 512, 128, True, "bf16")]
+    big = max(_lib.fa_bwd_workspace_size(sh.B, sh.Hq, sh.Hkv, sh.Nq, sh.Nkv, sh.d, int(det)) for sh in shapes)
+    ws = torch.empty(big, dtype=torch.uint8, device="cuda")
+    for i, shape in enumerate(shapes):
+        (q, k, v, do), _, _, g = oracle_full(shape, 12 + i)
+        qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+        o, lse = torch_api.forward(qd, kd, vd, shape.softmax_scale, shape.causal)
+        dq, dk, dv = torch_api.backward(qd, kd, vd, o, dod, lse, shape.softmax_scale, shape.causal, det, ws=ws)
+        torch.cuda.synchronize()
+        assert _lib.fa_last_device_error() == _lib.FA_OK
+        fails, rep = errors({"dQ": (_np(dq), g["dq"]), "dK": (_np(dk), g["dk"]), "dV": (_np(dv), g["dv"])})
+        assert not fails, f"call {i} {shape.name()}\n{rep}"
+
+
 def test_deterministic_is_bitwise_reproducible():
     shape = inputs.llama_gqa(1000)
     q, k, v, do = (t.cuda() for t in inputs.draw(shape, 8))
