@@ -318,7 +318,6 @@ fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t tO = tmem + lane_off + L::col_o(qt);
     const uint64_t sc2 = f2_bits(p.scale_log2, p.scale_log2);
     int g = 0;                   // S tiles of this query tile so far (P V of this tile committed so far)
-    int nx = 0;                  // items with work of this query tile
     bool ok = true;
     for (int k = 0, it = item_of(0); ok && it < p.items; it = item_of(++k)) {
       const Item w = decode(it, p);
@@ -455,7 +454,6 @@ fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(OFREE + qt));    // the next item's first P V may overwrite O
-      ++nx;
       if (row_ok && *abort_flag == 0) {
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
@@ -470,7 +468,6 @@ fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       }
     }
-    (void)nx;
   }
 
   tc_fence_before();
