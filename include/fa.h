@@ -149,7 +149,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  * row-wise dot product the pages precompute (flash_attention_backward.cu,
  * "Compute row-wise dot product: dO * O"; the D input of the Triton kernel in
  * triton #1806), -L*log2(e) per row, and (deterministic == 0) zeroes the fp32
- * dQ accumulator.  Writes only the workspace.
+ * dQ accumulator.  It also clears the workspace header: the call's abort word
+ * and the work-item counters of the persistent main and deterministic dQ
+ * kernels (each launch of those resets its counters when it completes; after a
+ * device-side failure, start again from this step).  Writes only the workspace.
  */
 int fa_bwd_preprocess(const void* o, const void* dO, const float* lse,
                       int B, int Hq, int Hkv, int Nq, int Nkv, int d, int dtype, int deterministic,
