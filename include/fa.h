@@ -159,13 +159,15 @@ int fa_bwd_preprocess(const void* o, const void* dO, const float* lse,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * fa_bwd_main -- step 2 of fa_bwd: the KV-tile-parallel kernel.  One CTA per
- * (128-row KV tile, key/value head, batch) walks every query tile of every
- * query head of its GQA group (triton #1806, "Minimal Repro": grid over
+ * fa_bwd_main -- step 2 of fa_bwd: the KV-tile-parallel kernel.  Each work
+ * item, a (128-row KV tile, key/value head, batch), walks every query tile of
+ * every query head of its GQA group (triton #1806, "Minimal Repro": grid over
  * (batch, head, KV block), loop over query blocks), recomputes S and P, and
  * accumulates dV += P^T dO and dK += dS^T Q on the tensor cores; dK, dV are
  * written once.  With deterministic == 0 it also forms dQ_tile = dS K and adds
- * it into the workspace accumulator.  Needs fa_bwd_preprocess first.
+ * it into the workspace accumulator.  Without a bias the items run on a
+ * persistent grid (one CTA per SM, items taken from a counter in the
+ * workspace); with one, one CTA per item.  Needs fa_bwd_preprocess first.
  */
 int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO,
                 void* dk, void* dv,
@@ -177,7 +179,8 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dO,
  * fa_bwd_dq -- step 3 of fa_bwd.  deterministic == 0: converts the fp32
  * accumulator to dq = scale * acc in the 16-bit dtype.  deterministic != 0:
  * runs the query-tile-parallel pass (flash_attention_backward.cu's
- * query-block grid with dQ kept on chip, "Compute dQ") and writes dq directly.
+ * query-block grid with dQ kept on chip, "Compute dQ"; persistent like
+ * fa_bwd_main when there is no bias) and writes dq directly.
  * Needs fa_bwd_preprocess (and, for deterministic == 0, fa_bwd_main) first.
  */
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
