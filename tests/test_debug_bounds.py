@@ -6,9 +6,10 @@ against the extents of its tensor, and a failed check records FA_ERR_BOUNDS and 
 the access.  A child process that loads this build instead of the normal one runs the
 forward and the backward (both dQ modes) on shapes that reach every check site --
 ragged tails, N = 1, GQA, Nq != Nkv, packed batches with empty sequences, strided
-(BSHD) tensors, additive bias with dBias -- and compares every output with the fp64
-oracle (max|err| <= 1e-2 * max|ref| + 1e-3).  The status word must stay FA_OK
-throughout: on valid inputs no check fires.
+(BSHD) tensors, additive bias with dBias, and the seeded sweep of mixed shapes of
+test_random_shapes.py -- and compares every output with the fp64 oracle
+(max|err| <= 1e-2 * max|ref| + 1e-3).  The status word must stay FA_OK throughout: on
+valid inputs no check fires.
 """
 import os
 import subprocess
@@ -27,7 +28,9 @@ sys.path.insert(0, {tests!r})
 sys.path.insert(0, {root!r})
 from attn_bwd_gb300 import _lib, inputs
 assert _lib.LIB_PATH.endswith("libattn_bwd_gb300_bounds.so"), _lib.LIB_PATH
-import test_parity, test_varlen, test_bias, test_strided
+import test_parity, test_varlen, test_bias, test_strided, test_random_shapes
+for shape in test_random_shapes._shapes():
+    test_random_shapes.test_random_shape(shape)
 for det in (False, True):
     test_parity.check_full(inputs.tiny_mha()[0], 1, det)
     for shape in inputs.ragged():
